@@ -1,0 +1,158 @@
+"""CPU oracle for the fused rank-sum + residual add + RMSNorm operator.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg call this package; the product path (the CUDA
+library ``libfarn.so`` and ``rank_sum_residual_gb300``) never imports it.
+
+The arithmetic lives in ``oracle.c`` (plain single-threaded C, fp32 with
+contraction off); this module only compiles it with gcc and marshals numpy
+arrays of bf16 bit patterns (``uint16``) into it.
+
+Method: FlagTree pull request "[TLERaw] Add NVSHMEM allreduce RMSNorm
+tutorial", Summary (the three-line contract) and Implementation section 3
+(residual + RMSNorm epilogue with FP32 accumulation).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+           "-fPIC", "-shared"]
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``src`` into the shared library ``out`` with gcc."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *_CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` next to its source if it is missing or stale."""
+    with _lock:
+        if (force or not os.path.exists(_LIB_PATH)
+                or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+            compile_oracle()
+    return _LIB_PATH
+
+
+def _declare(lib):
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f32_bits_to_bf16.argtypes = [ctypes.c_uint32]
+    lib.oracle_f32_bits_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_rank_sum.argtypes = [ctypes.POINTER(u16p), ctypes.c_int,
+                                    ctypes.c_int64, u16p]
+    lib.oracle_rank_sum.restype = None
+    lib.oracle_residual_add.argtypes = [u16p, u16p, ctypes.c_int64, u16p]
+    lib.oracle_residual_add.restype = None
+    lib.oracle_rmsnorm_row.argtypes = [u16p, u16p, ctypes.c_float,
+                                       ctypes.c_int64, u16p]
+    lib.oracle_rmsnorm_row.restype = ctypes.c_float
+    lib.oracle_forward.argtypes = [ctypes.POINTER(u16p), ctypes.c_int, u16p,
+                                   u16p, ctypes.c_float, ctypes.c_int64,
+                                   ctypes.c_int64, u16p, u16p, u16p]
+    lib.oracle_forward.restype = ctypes.c_int
+    return lib
+
+
+def load_library(path: str):
+    """Load an oracle shared library (the real one, or a test build)."""
+    return _declare(ctypes.CDLL(path))
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns as uint16, got {a.dtype}")
+    return a
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
+
+
+class Oracle:
+    """numpy front end over one loaded oracle library."""
+
+    def __init__(self, library=None):
+        self.lib = library if library is not None else lib()
+
+    def bf16_to_f32(self, b: int) -> float:
+        return float(self.lib.oracle_bf16_to_f32(int(b)))
+
+    def f32_to_bf16(self, f: float) -> int:
+        return int(self.lib.oracle_f32_to_bf16(float(np.float32(f))))
+
+    def f32_bits_to_bf16(self, u: int) -> int:
+        return int(self.lib.oracle_f32_bits_to_bf16(int(u) & 0xFFFFFFFF))
+
+    def rank_sum(self, xs) -> np.ndarray:
+        xs = [_u16(x) for x in xs]
+        n = xs[0].size
+        out = np.empty(xs[0].shape, np.uint16)
+        arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x) for x in xs])
+        self.lib.oracle_rank_sum(arr, len(xs), n, _p(out))
+        return out
+
+    def residual_add(self, reduced, residual) -> np.ndarray:
+        reduced, residual = _u16(reduced), _u16(residual)
+        out = np.empty(reduced.shape, np.uint16)
+        self.lib.oracle_residual_add(_p(reduced), _p(residual), reduced.size,
+                                     _p(out))
+        return out
+
+    def rmsnorm_row(self, ro, weight, eps: float):
+        ro, weight = _u16(ro), _u16(weight)
+        out = np.empty(ro.shape, np.uint16)
+        rstd = self.lib.oracle_rmsnorm_row(_p(ro), _p(weight), eps, ro.size,
+                                           _p(out))
+        return out, float(rstd)
+
+    def forward(self, xs, residual, weight, eps: float):
+        """All three outputs for W partials [T,H], residual [T,H], weight [H]."""
+        xs = [_u16(x) for x in xs]
+        residual, weight = _u16(residual), _u16(weight)
+        if residual.ndim != 2:
+            raise ValueError("residual must be [T, H]")
+        T, H = residual.shape
+        for x in xs:
+            if x.shape != (T, H):
+                raise ValueError("every partial must be [T, H] like residual")
+        if weight.shape != (H,):
+            raise ValueError("weight must be [H]")
+        reduced = np.empty((T, H), np.uint16)
+        ro = np.empty((T, H), np.uint16)
+        norm = np.empty((T, H), np.uint16)
+        arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x) for x in xs])
+        rc = self.lib.oracle_forward(arr, len(xs), _p(residual), _p(weight),
+                                     eps, T, H, _p(reduced), _p(ro), _p(norm))
+        if rc != 0:
+            raise ValueError(f"oracle_forward rejected its arguments (rc={rc})")
+        return reduced, ro, norm
+
+
+def forward(xs, residual, weight, eps: float):
+    """Module-level shorthand for ``Oracle().forward``."""
+    return Oracle().forward(xs, residual, weight, eps)

@@ -1,0 +1,164 @@
+/*
+ * Oracle for the fused rank-sum + residual add + RMSNorm operator.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, single-threaded
+ * CPU statement of what the operator computes.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg load it; the product path
+ * (the CUDA library and its Python binding) never does, and shares no code,
+ * header or constant with it.
+ *
+ * Source of the method: FlagTree pull request "[TLERaw] Add NVSHMEM
+ * allreduce RMSNorm tutorial".
+ *   - Summary: the contract
+ *         reduced      = AllReduce_SUM(x)
+ *         residual_out = reduced + residual
+ *         norm_out     = RMSNorm(residual_out, weight, eps)
+ *   - Implementation section 3, "Residual + RMSNorm epilogue": the epilogue
+ *     runs after the reduction is complete, on `reduced`, with FP32
+ *     accumulation for the normalisation.
+ *   - Correctness section: all tensors are BF16.
+ *
+ * Readings where the page is silent (each one is listed with its reason in
+ * the design notes of this repository):
+ *   1. The W partials are summed in FP32, strictly in rank order 0..W-1,
+ *      with the accumulator seeded from the widened x[0] (not from +0.0,
+ *      which would turn an all -0 column into +0).
+ *   2. `reduced` is rounded to bf16 before the residual is added (the
+ *      epilogue consumes the reduced tensor, itself a bf16 output).
+ *   3. residual_out = bf16(f32(reduced) + f32(residual)).
+ *   4. RMSNorm over the bf16 residual_out of one row (H elements):
+ *         ss   = sum over h of ro[h]*ro[h]   (fp32, sequential in h)
+ *         mean = ss / H                      (fp32 division)
+ *         rstd = 1 / sqrt(mean + eps)        (fp32, eps inside the root)
+ *         norm_out[h] = bf16((ro[h] * rstd) * weight[h])
+ *      i.e. the weight multiplies the fp32 normalised value and the result
+ *      is rounded once.
+ *   5. Every fp32 -> bf16 conversion rounds to nearest, ties to even.
+ *      Subnormals are kept.  NaN stays NaN (quiet, sign kept).
+ *
+ * Build: -O2 -ffp-contract=off, no fast-math, so that every + and * above
+ * is one IEEE single-precision operation (no fused multiply-add, no
+ * reassociation).  sqrtf and '/' are IEEE correctly rounded.
+ *
+ * bf16 values travel as their 16-bit patterns (uint16_t).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* bfloat16 is the upper half of an IEEE binary32 pattern (1 sign bit,
+ * 8 exponent bits, 7 fraction bits), so widening is exact: shift the
+ * 16 bits into the upper half of a binary32 and zero the rest. */
+float oracle_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Narrowing binary32 -> bfloat16, round to nearest, ties to even.
+ * The 16 dropped low bits decide: above half an ulp rounds up, below
+ * rounds down, exactly half rounds to the even kept pattern.  Rounding up
+ * adds one to the kept pattern; a carry out of the fraction moves into the
+ * exponent, which is the correct next representable value (up to +-inf).
+ * NaN is returned as a quiet NaN with the same sign. */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t kept = u >> 16;
+    uint32_t dropped = u & 0xFFFFu;
+    if (isnan(f))
+        return (uint16_t)(kept | 0x0040u);
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+/* The same narrowing applied to a binary32 given by its bit pattern, so a
+ * caller can pass any NaN payload unchanged. */
+uint16_t oracle_f32_bits_to_bf16(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return oracle_f32_to_bf16(f);
+}
+
+/* Step a1, rank sum of one element position: FP32 accumulation in rank
+ * order, the sum rounded to bf16. */
+static uint16_t rank_sum_one(const uint16_t *const *x, int W, int64_t idx)
+{
+    float acc = oracle_bf16_to_f32(x[0][idx]);
+    for (int r = 1; r < W; ++r)
+        acc = acc + oracle_bf16_to_f32(x[r][idx]);
+    return oracle_f32_to_bf16(acc);
+}
+
+/* Step a1 over a [T,H] block: reduced[t,h] = bf16(sum_r x[r][t,h]). */
+void oracle_rank_sum(const uint16_t *const *x, int W, int64_t n,
+                     uint16_t *reduced)
+{
+    for (int64_t i = 0; i < n; ++i)
+        reduced[i] = rank_sum_one(x, W, i);
+}
+
+/* Step a2: residual_out = bf16(f32(reduced) + f32(residual)). */
+void oracle_residual_add(const uint16_t *reduced, const uint16_t *residual,
+                         int64_t n, uint16_t *residual_out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float s = oracle_bf16_to_f32(reduced[i]) + oracle_bf16_to_f32(residual[i]);
+        residual_out[i] = oracle_f32_to_bf16(s);
+    }
+}
+
+/* Steps a3-a4 for one row of H elements: RMSNorm of the bf16 residual_out
+ * with FP32 accumulation, scaled by weight, rounded once to bf16.
+ * Returns the fp32 rstd it used (the tests read it). */
+float oracle_rmsnorm_row(const uint16_t *ro, const uint16_t *weight,
+                         float eps, int64_t H, uint16_t *norm_out)
+{
+    float ss = 0.0f;
+    for (int64_t h = 0; h < H; ++h) {
+        float v = oracle_bf16_to_f32(ro[h]);
+        ss = ss + v * v;
+    }
+    float mean = ss / (float)H;
+    float rstd = 1.0f / sqrtf(mean + eps);
+    for (int64_t h = 0; h < H; ++h) {
+        float v = oracle_bf16_to_f32(ro[h]);
+        float n = v * rstd;
+        norm_out[h] = oracle_f32_to_bf16(n * oracle_bf16_to_f32(weight[h]));
+    }
+    return rstd;
+}
+
+/* The whole operator on row-major [T,H] tensors, row after row, in the
+ * order of the contract: rank sum, residual add, RMSNorm.
+ * x is an array of W pointers, one per rank partial.  Returns 0, or -1 on
+ * an argument it cannot process (W < 1, T < 0, H < 1, a null pointer). */
+int oracle_forward(const uint16_t *const *x, int W, const uint16_t *residual,
+                   const uint16_t *weight, float eps, int64_t T, int64_t H,
+                   uint16_t *reduced, uint16_t *residual_out,
+                   uint16_t *norm_out)
+{
+    if (W < 1 || T < 0 || H < 1 || !x || !residual || !weight || !reduced ||
+        !residual_out || !norm_out)
+        return -1;
+    for (int r = 0; r < W; ++r)
+        if (!x[r])
+            return -1;
+    const uint16_t *row_x[256];
+    if (W > 256)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t off = t * H;
+        for (int r = 0; r < W; ++r)
+            row_x[r] = x[r] + off;
+        oracle_rank_sum(row_x, W, H, reduced + off);
+        oracle_residual_add(reduced + off, residual + off, H, residual_out + off);
+        oracle_rmsnorm_row(residual_out + off, weight, eps, H, norm_out + off);
+    }
+    return 0;
+}

@@ -1,0 +1,215 @@
+"""Seeded synthetic inputs for the fused rank-sum + residual + RMSNorm operator.
+
+A module of its own: it makes input bytes and nothing else.  Both the CUDA
+path (device fill through ``libfarn_synth.so``) and the CPU oracle's tests
+(the numpy twin below) draw their inputs here; it contains none of the
+operator's arithmetic.
+
+Recipe (the same on device and host): a SplitMix64 counter stream per
+(seed, stream_id), Box-Muller normals or uniforms evaluated in fp64, an
+optional outlier multiplier, fp64 -> fp32 round-to-nearest, then bf16 by
+truncating the fp32 pattern to its upper 16 bits.  ``gen.cu`` states the
+constants.  The host twin uses numpy's log/cos, the device CUDA's, so the two
+can differ in a rare last bit; parity never depends on that, because every
+GPU parity test feeds the oracle the bytes the device generated.
+
+Workloads follow the operator page's setting (bf16 partials of W tensor-
+parallel ranks, hidden sizes of LLM layers) at the sizes of the five
+benchmark shapes below.  "N(m, v)" is read as mean m and VARIANCE v.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gen.cu")
+_LIB_PATH = os.path.join(_HERE, "libfarn_synth.so")
+_lock = threading.Lock()
+_lib = None
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+NORMAL, UNIFORM = 0, 1
+STREAM_RESIDUAL, STREAM_WEIGHT = 1000, 1001
+
+
+# --------------------------------------------------------------------- recipes
+@dataclass(frozen=True)
+class Dist:
+    kind: int            # NORMAL or UNIFORM
+    p0: float            # mean, or lower bound
+    p1: float            # variance, or upper bound
+    outlier_p: float = 0.0
+    outlier_scale: float = 1.0
+
+    def describe(self) -> str:
+        if self.kind == NORMAL:
+            s = f"N(mean={self.p0}, var={self.p1:g}, sigma={self.p1 ** 0.5:.4f})"
+        else:
+            s = f"U({self.p0}, {self.p1})"
+        if self.outlier_p > 0:
+            s += f" with {self.outlier_p:g} of entries x{self.outlier_scale:g}"
+        return s
+
+
+@dataclass(frozen=True)
+class Problem:
+    """One operator call: W partials [T,H], residual [T,H], weight [H]."""
+    name: str
+    W: int
+    T: int
+    H: int
+    eps: float
+    seed: int
+    x: Dist
+    residual: Dist = Dist(NORMAL, 0.0, 1.0)
+    weight: Dist = Dist(NORMAL, 1.0, 0.1)
+
+    def algorithmic_bytes(self) -> int:
+        """(W+1)*T*H*2 read + H*2 weight + 3*T*H*2 written."""
+        return (self.W + 1) * self.T * self.H * 2 + self.H * 2 + 3 * self.T * self.H * 2
+
+    def with_seed(self, seed: int) -> "Problem":
+        return Problem(self.name, self.W, self.T, self.H, self.eps, seed,
+                       self.x, self.residual, self.weight)
+
+    def with_T(self, T: int) -> "Problem":
+        return Problem(f"{self.name.split('@')[0]}@T{T}", self.W, T, self.H,
+                       self.eps, self.seed, self.x, self.residual, self.weight)
+
+
+N01 = Dist(NORMAL, 0.0, 1.0)
+DECODE_TS = (1, 2, 4, 8, 16, 32, 64, 128)
+
+
+def _decode(T: int) -> Problem:
+    return Problem(f"decode@T{T}", 8, T, 4096, 1e-5, T, N01)
+
+
+WORKLOADS = {
+    "c1": [Problem("c1", 4, 16, 2048, 1e-6, 0, N01)],
+    "decode": [_decode(T) for T in DECODE_TS],
+    "prefill": [Problem("prefill", 8, 8192, 8192, 1e-6, 0,
+                        Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
+                        N01, Dist(UNIFORM, 0.5, 1.5))],
+    "nonpow2": [Problem("nonpow2", 4, 32768, 5120, 1e-6, 0, N01)],
+    "wide": [Problem("wide", 16, 4096, 7168, 1e-6, 0, Dist(NORMAL, 0.0, 1.0 / 16))],
+}
+
+
+def workload(name: str) -> list[Problem]:
+    if name not in WORKLOADS:
+        raise KeyError(f"unknown workload {name!r}; have {sorted(WORKLOADS)}")
+    return WORKLOADS[name]
+
+
+# ------------------------------------------------------------------ host twin
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = z ^ (z >> np.uint64(30))
+    z = z * np.uint64(0xBF58476D1CE4E5B9)
+    z = z ^ (z >> np.uint64(27))
+    z = z * np.uint64(0x94D049BB133111EB)
+    z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def _base(seed: int, stream_id: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        s = np.array([stream_id], np.uint64) + GAMMA
+        return _mix64(np.array([seed], np.uint64) ^ _mix64(s))[0]
+
+
+def _unit(z: np.ndarray) -> np.ndarray:
+    return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * 2.0 ** -53
+
+
+def host_bf16(n: int, seed: int, stream_id: int, dist: Dist) -> np.ndarray:
+    """The recipe evaluated with numpy; returns n bf16 patterns (uint16)."""
+    with np.errstate(over="ignore"):
+        base = _base(seed, stream_id)
+        j = np.arange(n, dtype=np.uint64) * np.uint64(3)
+        u1 = _unit(_mix64(base + (j + np.uint64(1)) * GAMMA))
+        u2 = _unit(_mix64(base + (j + np.uint64(2)) * GAMMA))
+        if dist.kind == NORMAL:
+            v = dist.p0 + np.sqrt(dist.p1) * (np.sqrt(-2.0 * np.log(u1))
+                                              * np.cos(2.0 * np.pi * u2))
+        else:
+            v = dist.p0 + (dist.p1 - dist.p0) * u1
+        if dist.outlier_p > 0:
+            u3 = _unit(_mix64(base + (j + np.uint64(3)) * GAMMA))
+            v = np.where(u3 < dist.outlier_p, v * dist.outlier_scale, v)
+    f = v.astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def host_inputs(p: Problem):
+    """(partials list of [T,H], residual [T,H], weight [H]) as uint16 arrays."""
+    n = p.T * p.H
+    xs = [host_bf16(n, p.seed, r, p.x).reshape(p.T, p.H) for r in range(p.W)]
+    res = host_bf16(n, p.seed, STREAM_RESIDUAL, p.residual).reshape(p.T, p.H)
+    w = host_bf16(p.H, p.seed, STREAM_WEIGHT, p.weight)
+    return xs, res, w
+
+
+# ---------------------------------------------------------------- device fill
+def build(force: bool = False) -> str:
+    """Compile libfarn_synth.so for sm_103a next to its source."""
+    with _lock:
+        if (force or not os.path.exists(_LIB_PATH)
+                or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            subprocess.run(
+                ["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                 "-lineinfo", "-Xcompiler", "-fPIC", "-shared", "-o", tmp, _SRC],
+                check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built; call synth.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.farn_synth_fill_bf16.argtypes = [
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
+            ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+            ctypes.c_double, ctypes.c_void_p]
+        lib.farn_synth_fill_bf16.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def fill_device(t, seed: int, stream_id: int, dist: Dist, stream=None) -> None:
+    """Fill a contiguous torch bf16 CUDA tensor in place with the recipe."""
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("fill_device wants a contiguous bf16 CUDA tensor")
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    rc = _load().farn_synth_fill_bf16(
+        t.data_ptr(), t.numel(), seed, stream_id, dist.kind, dist.p0, dist.p1,
+        dist.outlier_p, dist.outlier_scale, s.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"farn_synth_fill_bf16 failed (rc={rc})")
+
+
+def device_inputs(p: Problem, device="cuda", seed: int | None = None):
+    """Allocate and fill (partials, residual, weight) on the device."""
+    import torch
+    sd = p.seed if seed is None else seed
+    xs = []
+    for r in range(p.W):
+        t = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=device)
+        fill_device(t, sd, r, p.x)
+        xs.append(t)
+    res = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=device)
+    fill_device(res, sd, STREAM_RESIDUAL, p.residual)
+    w = torch.empty((p.H,), dtype=torch.bfloat16, device=device)
+    fill_device(w, sd, STREAM_WEIGHT, p.weight)
+    return xs, res, w

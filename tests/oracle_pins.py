@@ -1,0 +1,287 @@
+"""Pins for the CPU oracle: checks against facts the oracle does not compute.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when
+the oracle disagrees with a hand-computed golden value, an exact rational
+result, a closed form, an invariant, or a float64 brute force.  The same
+pins run against the real oracle (they must all pass) and against mutated
+copies of it (each mutant must fail at least one), see
+test_oracle_mutants.py.
+
+Method: FlagTree pull request "[TLERaw] Add NVSHMEM allreduce RMSNorm
+tutorial", Summary (contract) and Implementation section 3 (epilogue).
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import bf16_exact as bx
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "hand_rows.txt")
+
+
+# ------------------------------------------------------------------- goldens
+def load_golden(path: str = GOLDEN) -> dict:
+    cases, cur = {}, None
+    with open(path) as fh:
+        for raw in fh:
+            line = raw.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("[") and line.endswith("]"):
+                cur = cases.setdefault(line[1:-1], {})
+                continue
+            k, v = (s.strip() for s in line.split("=", 1))
+            cur[k] = v
+    return cases
+
+
+def _row(s: str) -> np.ndarray:
+    return np.array([bx.bits(t) for t in s.split()], np.uint16)
+
+
+def _compare(name, key, got, want):
+    got = np.asarray(got).ravel()
+    nan_w = bx.nan_mask(want)
+    assert np.array_equal(bx.nan_mask(got), nan_w), f"{name}.{key}: NaN positions {got} vs {want}"
+    ok = np.where(nan_w, True, got == want)
+    assert ok.all(), f"{name}.{key}: got {[hex(v) for v in got]} want {[hex(v) for v in want]}"
+
+
+def pin_golden_cases(O):
+    for name, c in load_golden().items():
+        xs = []
+        r = 0
+        while f"x{r}" in c:
+            xs.append(_row(c[f"x{r}"])[None, :])
+            r += 1
+        res = _row(c["residual"])[None, :]
+        w = _row(c["weight"])
+        eps = float(c["eps"])
+        red, ro, nrm = O.forward(xs, res, w, eps)
+        for key, got in (("reduced", red), ("residual_out", ro), ("norm_out", nrm)):
+            if key in c:
+                _compare(name, key, got, _row(c[key]))
+
+
+# ------------------------------------------------------- format conversions
+def pin_bf16_widening_all_patterns(O):
+    for b in range(0, 1 << 16, 7):            # every 7th pattern, all classes
+        v = O.bf16_to_f32(b)
+        d = bx.decode(b)
+        if isinstance(d, float):
+            if np.isnan(d):
+                assert np.isnan(v), hex(b)
+            else:
+                assert v == d, hex(b)
+        else:
+            assert Fraction(v) == d, hex(b)
+    for b in (0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x7F7F, 0xFF7F,
+              0x7F80, 0xFF80, 0x3F80, 0xBF80):
+        d = bx.decode(b)
+        v = O.bf16_to_f32(b)
+        assert (Fraction(v) == d) if not isinstance(d, float) else (v == d), hex(b)
+    assert np.signbit(O.bf16_to_f32(0x8000))
+
+
+def _f32_from_bits(u: int) -> float:
+    return float(np.array([u], np.uint32).view(np.float32)[0])
+
+
+def pin_bf16_rounding_vs_exact(O):
+    rng = np.random.default_rng(1234)
+    pats = list(rng.integers(0, 1 << 32, 4000, dtype=np.uint64))
+    # ties, just-below/above ties, subnormals, overflow edge, specials
+    for hi in (0x3F80, 0x3F81, 0xBF80, 0x0000, 0x0001, 0x7F7F, 0x8080, 0x4B80):
+        for lo in (0x0000, 0x7FFF, 0x8000, 0x8001, 0xFFFF):
+            pats.append((hi << 16) | lo)
+    pats += [0x7F800000, 0xFF800000, 0x7F800001, 0xFF800001, 0x7FC00000,
+             0x7F7FFFFF, 0x7F7F8000, 0x7F7F7FFF, 0x00000001, 0x80000001]
+    for u in pats:
+        u = int(u)
+        f = _f32_from_bits(u)
+        got = O.f32_bits_to_bf16(u)
+        if np.isnan(f):
+            assert bx.is_nan(got), (hex(u), hex(got))
+            assert (got & 0x8000) == (u >> 16 & 0x8000), "NaN sign kept"
+            continue
+        want = bx.round_rne(f if (f == 0 or np.isinf(f)) else Fraction(f))
+        assert got == want, (hex(u), hex(got), hex(want))
+
+
+def pin_overflow_and_subnormal(O):
+    mx = np.array([[0x7F7F]], np.uint16)
+    red, _, _ = O.forward([mx, mx], np.zeros((1, 1), np.uint16),
+                          np.array([bx.bits(1)], np.uint16), 1e-6)
+    assert red[0, 0] == bx.POS_INF, hex(red[0, 0])
+    tiny = np.array([[0x0001, 0x8001]], np.uint16)          # +-2^-133
+    red, _, _ = O.forward([tiny, tiny], np.zeros((1, 2), np.uint16),
+                          np.array([bx.bits(1)] * 2, np.uint16), 1e-6)
+    assert list(red[0]) == [0x0002, 0x8002], [hex(v) for v in red[0]]
+
+
+# ------------------------------------------------------------- rank sum (a1)
+def pin_rank_sum_integers(O):
+    """Integer-valued partials: the exact integer sum, rounded once."""
+    rng = np.random.default_rng(7)
+    for W in (1, 2, 3, 5, 8, 16, 32):
+        vals = rng.integers(-128, 129, size=(W, 257))
+        xs = [np.array([bx.bits(int(v)) for v in row], np.uint16) for row in vals]
+        got = O.rank_sum(xs)
+        want = [bx.round_rne(Fraction(int(s))) if s != 0 else 0
+                for s in vals.sum(axis=0)]
+        assert list(got) == want, f"W={W}"
+
+
+def _fp32_exact(q: Fraction) -> bool:
+    f = np.float32(float(q))
+    return Fraction(float(f)) == q
+
+
+def pin_rank_sum_brute_force(O):
+    """bf16 partials of mixed magnitude: compare with the exact rational sum.
+
+    Where every prefix sum is exact in fp32 the oracle must give the exact
+    sum rounded once; elsewhere fp32 rounding can move it by at most 1 ulp."""
+    rng = np.random.default_rng(11)
+    n_exact = 0
+    for W in (2, 3, 4):
+        mags = rng.normal(size=(W, 600)) * np.exp2(rng.integers(-12, 12, (W, 600)))
+        xs = [((m.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)) for m in mags]
+        got = O.rank_sum(xs)
+        for i in range(got.size):
+            terms = [bx.decode(int(x[i])) for x in xs]
+            prefix, exact = terms[0], True
+            for t in terms[1:]:
+                prefix = prefix + t
+                exact &= _fp32_exact(prefix)
+            want = bx.round_rne(prefix) if prefix != 0 else int(got[i]) & 0x8000
+            if exact:
+                n_exact += 1
+                assert int(got[i]) == want or (prefix == 0 and (int(got[i]) & 0x7FFF) == 0), \
+                    (W, i, hex(int(got[i])), hex(want))
+            else:
+                assert bx.ulp_diff(int(got[i]), want) <= 1, (W, i)
+    assert n_exact > 1000
+
+
+# ----------------------------------------------------------- residual (a2)
+def pin_residual_add_brute_force(O):
+    rng = np.random.default_rng(5)
+    a = (rng.normal(size=3000) * np.exp2(rng.integers(-20, 20, 3000))).astype(np.float32)
+    b = (rng.normal(size=3000) * np.exp2(rng.integers(-20, 20, 3000))).astype(np.float32)
+    ab = (a.view(np.uint32) >> 16).astype(np.uint16)
+    bb = (b.view(np.uint32) >> 16).astype(np.uint16)
+    got = O.residual_add(ab, bb)
+    for i in range(got.size):
+        s = bx.decode(int(ab[i])) + bx.decode(int(bb[i]))
+        if s == 0:
+            assert (int(got[i]) & 0x7FFF) == 0
+            continue
+        want = bx.round_rne(s)
+        if _fp32_exact(s):
+            assert int(got[i]) == want, (i, hex(int(got[i])), hex(want))
+        else:
+            assert bx.ulp_diff(int(got[i]), want) <= 1
+
+
+def pin_residual_adds_rounded_reduced(O):
+    """The residual is added to the bf16-rounded reduced value: x = (1, 2^-8)
+    gives reduced 1.0 (tie to even); + residual 2^-8 -> 1 + 2^-8 -> 1.0 again.
+    Adding to the unrounded fp32 sum would give 1 + 2^-7 = 1.0078125."""
+    one, q = bx.bits(1), bx.bits(Fraction(1, 256))
+    xs = [np.array([[one]], np.uint16), np.array([[q]], np.uint16)]
+    red, ro, _ = O.forward(xs, np.array([[q]], np.uint16),
+                           np.array([one], np.uint16), 1e-6)
+    assert red[0, 0] == one and ro[0, 0] == one, (hex(red[0, 0]), hex(ro[0, 0]))
+
+
+# --------------------------------------------------------- RMSNorm (a3, a4)
+def pin_rmsnorm_float64_brute_force(O):
+    """Recompute the normalisation in float64 from the oracle's residual_out,
+    round once: the oracle's fp32 result must be within 1 bf16 ulp."""
+    rng = np.random.default_rng(3)
+    for T, H, W in ((1, 1, 1), (3, 7, 2), (8, 64, 16), (5, 33, 4), (2, 64, 3)):
+        xs = [(rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16)
+              .astype(np.uint16) for _ in range(W)]
+        res = (rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        w = (rng.uniform(0.5, 1.5, H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        eps = 1e-5
+        _, ro, nrm = O.forward(xs, res, w, eps)
+        r64 = bx.to_f64(ro)
+        rstd = 1.0 / np.sqrt((r64 * r64).mean(axis=1, keepdims=True) + float(np.float32(eps)))
+        want = bx.from_f64_rne(r64 * rstd * bx.to_f64(w)[None, :])
+        d = bx.ulp_diff(nrm, want)
+        assert d.max() <= 1, (T, H, W, int(d.max()))
+
+
+def pin_rstd_closed_form(O):
+    """rstd of a row = 1/sqrt(mean(ro^2) + eps) to fp32 accuracy."""
+    rng = np.random.default_rng(9)
+    for H in (4, 37, 256):
+        ro = (rng.normal(size=H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        w = np.full(H, bx.bits(1), np.uint16)
+        _, rstd = O.rmsnorm_row(ro, w, 1e-6)
+        r64 = bx.to_f64(ro)
+        exact = 1.0 / np.sqrt((r64 * r64).mean() + float(np.float32(1e-6)))
+        assert abs(rstd / exact - 1) < 4e-6 + 1e-7 * H, (H, rstd, exact)
+
+
+def pin_scale_invariance(O):
+    """With eps = 0, scaling the input by 2 or 4 scales residual_out exactly
+    and leaves norm_out bit-identical (power-of-two scaling is exact through
+    square, sum, division by H, sqrt and reciprocal)."""
+    rng = np.random.default_rng(21)
+    for H in (64, 2048):
+        x = rng.normal(size=(3, H)).astype(np.float32)
+        w = (rng.normal(1.0, 0.3, H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        base = None
+        for s in (1.0, 2.0, 4.0):
+            xb = ((x * np.float32(s)).view(np.uint32) >> 16).astype(np.uint16)
+            red, ro, nrm = O.forward([xb], np.zeros((3, H), np.uint16), w, 0.0)
+            if base is None:
+                base = (ro, nrm)
+            else:
+                assert np.array_equal(bx.to_f64(ro), bx.to_f64(base[0]) * s)
+                assert np.array_equal(nrm, base[1]), f"H={H} s={s}"
+
+
+def pin_unit_mean_square(O):
+    """weight = 1 and mean(ro^2) >> eps: mean(norm_out^2) = 1 up to rounding."""
+    rng = np.random.default_rng(4)
+    H = 4096
+    xs = [(rng.normal(size=(4, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(4)]
+    res = (rng.normal(size=(4, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = np.full(H, bx.bits(1), np.uint16)
+    _, _, nrm = O.forward(xs, res, w, 1e-6)
+    ms = (bx.to_f64(nrm) ** 2).mean(axis=1)
+    assert np.all(np.abs(ms - 1.0) < 2.0 ** -7), ms
+
+
+def pin_row_tiling_independent(O):
+    """Rows are independent: one call over T rows equals per-block calls."""
+    rng = np.random.default_rng(8)
+    T, H, W = 9, 40, 3
+    xs = [(rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(W)]
+    res = (rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = (rng.normal(1, .1, H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    full = O.forward(xs, res, w, 1e-6)
+    for lo, hi in ((0, 1), (1, 5), (5, 9)):
+        part = O.forward([x[lo:hi] for x in xs], res[lo:hi], w, 1e-6)
+        for a, b in zip(full, part):
+            assert np.array_equal(a[lo:hi], b)
+    # and each row on its own against the step functions
+    for t in range(T):
+        red = O.rank_sum([x[t] for x in xs])
+        ro = O.residual_add(red, res[t])
+        nrm, _ = O.rmsnorm_row(ro, w, 1e-6)
+        assert np.array_equal(red, full[0][t]) and np.array_equal(ro, full[1][t])
+        assert np.array_equal(nrm, full[2][t])
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

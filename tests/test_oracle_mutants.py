@@ -1,0 +1,71 @@
+"""Planted mistakes: each mutant is a copy of oracle.c with one plausible
+error (a dropped term, a wrong sign, order or index, a different rounding),
+compiled on the CPU.  The pins must catch every one of them; a mutant that
+passes every pin would mean the pins cannot tell that mistake apart."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "reverse_rank_order": (
+        "for (int r = 1; r < W; ++r)\n        acc = acc + oracle_bf16_to_f32(x[r][idx]);",
+        "for (int r = W - 1; r >= 1; --r)\n        acc = acc + oracle_bf16_to_f32(x[r][idx]);"),
+    "seed_with_positive_zero": (
+        "float acc = oracle_bf16_to_f32(x[0][idx]);\n    for (int r = 1;",
+        "float acc = 0.0f;\n    for (int r = 0;"),
+    "subtract_partial": (
+        "acc = acc + oracle_bf16_to_f32(x[r][idx]);",
+        "acc = acc - oracle_bf16_to_f32(x[r][idx]);"),
+    "wrong_partial_index": (
+        "acc = acc + oracle_bf16_to_f32(x[r][idx]);",
+        "acc = acc + oracle_bf16_to_f32(x[0][idx]);"),
+    "drop_residual": (
+        "oracle_bf16_to_f32(reduced[i]) + oracle_bf16_to_f32(residual[i])",
+        "oracle_bf16_to_f32(reduced[i])"),
+    "ties_away_from_zero": (
+        "(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
+    "truncate_instead_of_round": (
+        "kept += 1u;", "kept += 0u;"),
+    "nan_not_quieted": (
+        "return (uint16_t)(kept | 0x0040u);", "return (uint16_t)kept;"),
+    "eps_outside_root": (
+        "1.0f / sqrtf(mean + eps)", "1.0f / (sqrtf(mean) + eps)"),
+    "no_division_by_H": (
+        "float mean = ss / (float)H;", "float mean = ss;"),
+    "sum_not_squared": (
+        "ss = ss + v * v;", "ss = ss + v;"),
+    "weight_dropped": (
+        "oracle_f32_to_bf16(n * oracle_bf16_to_f32(weight[h]))",
+        "oracle_f32_to_bf16(n)"),
+    "weight_index_fixed": (
+        "oracle_bf16_to_f32(weight[h])", "oracle_bf16_to_f32(weight[0])"),
+    "divide_instead_of_multiply": (
+        "float n = v * rstd;", "float n = v / rstd;"),
+    "row_offset_wrong": (
+        "int64_t off = t * H;", "int64_t off = t * (H - 1);"),
+    "widen_drops_low_bit": (
+        "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)(b & 0xFFFEu)) << 16;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.load_library(oracle.compile_oracle(str(src), str(tmp_path / "libmutant.so")))
+    O = oracle.Oracle(lib)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(O)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"mutant {name} passed every pin"
