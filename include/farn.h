@@ -1,0 +1,131 @@
+/*
+ * farn.h - fused rank-sum + residual add + RMSNorm on one GB300 (sm_103a).
+ *
+ * The operation is the contract of FlagTree pull request "[TLERaw] Add
+ * NVSHMEM allreduce RMSNorm tutorial" (Summary):
+ *
+ *     reduced      = sum over ranks r = 0..W-1 of x[r]
+ *     residual_out = reduced + residual
+ *     norm_out     = RMSNorm(residual_out, weight, eps)
+ *
+ * with the epilogue of its Implementation section 3 (residual add, then
+ * RMSNorm with FP32 accumulation) fused into the same kernel.  On one GPU
+ * the W partials of the page's all-reduce are W bf16 tensors that already
+ * sit in this GPU's memory; the library reads them through a pointer array,
+ * so there is no collective and no cross-GPU traffic.
+ *
+ * Arithmetic (element (t,h); f() widens bf16 to fp32 exactly, bf16()
+ * rounds fp32 to nearest even):
+ *     reduced[t,h]      = bf16(f(x[0]) + f(x[1]) + ... + f(x[W-1]))   fp32, rank order
+ *     residual_out[t,h] = bf16(f(reduced[t,h]) + f(residual[t,h]))
+ *     rstd[t]           = 1 / sqrt(sum_h f(residual_out[t,h])^2 / H + eps)
+ *     norm_out[t,h]     = bf16((f(residual_out[t,h]) * rstd[t]) * f(weight[h]))
+ * reduced and residual_out are exact functions of the inputs (bit for bit
+ * the same on every launch configuration); norm_out depends on the
+ * summation order of the row's sum of squares and may differ by one bf16
+ * ulp between launch configurations.
+ *
+ * Layout: every [T,H] tensor is row-major and contiguous (row t starts at
+ * element t*H), bf16 (2-byte IEEE bfloat16 patterns).  weight is [H].
+ * All tensor pointers are DEVICE pointers on the context's device, owned
+ * by the caller; the library keeps none of them after a call returns.
+ * The fast kernels need every pointer 16-byte aligned and H a multiple
+ * of 8; other shapes and alignments are served by a slower kernel.
+ *
+ * Errors: every entry point returns FARN_OK (0) or a negative farn_status.
+ * On an error nothing is launched and no output is written.
+ * Launch-time CUDA errors are reported; errors of the asynchronous kernel
+ * itself surface at the caller's next synchronisation, as usual in CUDA.
+ */
+#ifndef FARN_H_
+#define FARN_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest number of rank partials one call accepts. */
+#define FARN_MAX_W 32
+
+typedef enum {
+    FARN_OK = 0,
+    FARN_ERR_INVALID_ARG = -1,  /* null pointer, W/T/H/eps out of range     */
+    FARN_ERR_UNSUPPORTED = -2,  /* shape the library cannot launch           */
+    FARN_ERR_ALIAS = -3,        /* an output overlaps an input or an output  */
+    FARN_ERR_CUDA = -4,         /* CUDA runtime error (launch, device query) */
+    FARN_ERR_NOMEM = -5         /* host allocation of the context failed     */
+} farn_status;
+
+/* Opaque per-device context: device properties and kernel attributes
+ * queried once.  Immutable after farn_create; one context may serve any
+ * number of streams and host threads at once. */
+typedef struct farn_ctx farn_ctx;
+
+/* Create a context for CUDA device `device` (this is the one-time set-up
+ * that the page's host side does at initialisation, Implementation
+ * section 4, "host-side C ABI"; there is no communicator to bootstrap).
+ * Queries the SM count and cluster limits and sets kernel attributes.
+ * Enqueues no work and allocates no device memory.  The caller's current
+ * device is left as it was.
+ * Returns FARN_ERR_INVALID_ARG if out is NULL or device < 0,
+ * FARN_ERR_CUDA if the device cannot be queried, FARN_ERR_NOMEM. */
+int farn_create(farn_ctx **out, int device);
+
+/* The fused operator on `stream` (asynchronous; the call does not wait
+ * for the GPU).
+ *   partials     host array of W device pointers, partials[r] -> x[r],
+ *                bf16 [T,H]; the array itself is read during the call only.
+ *   W            1 .. FARN_MAX_W
+ *   residual     bf16 [T,H]
+ *   weight       bf16 [H]
+ *   eps          finite, >= 0 (fp32; added to the mean square inside sqrt)
+ *   T            rows (tokens), >= 0; T == 0 returns FARN_OK, launches nothing
+ *   H            hidden size (row length), >= 1
+ *   reduced_out, residual_out, norm_out   bf16 [T,H] outputs
+ *   stream       CUDA stream (0 = legacy default stream)
+ * Outputs may not overlap each other or any input, with one exception:
+ * residual_out may be exactly residual (in-place residual update).
+ * Returns FARN_ERR_INVALID_ARG (ctx or a pointer NULL, W, T, H or eps out
+ * of range, T*H*2 bytes overflowing), FARN_ERR_ALIAS, FARN_ERR_UNSUPPORTED,
+ * or FARN_ERR_CUDA if the launch failed. */
+int farn_forward(const farn_ctx *ctx,
+                 const void *const *partials, int W,
+                 const void *residual, const void *weight, float eps,
+                 int64_t T, int64_t H,
+                 void *reduced_out, void *residual_out, void *norm_out,
+                 cudaStream_t stream);
+
+/* The argument checks of farn_forward alone, on the host: no CUDA call, no
+ * launch, pointers are only compared, never dereferenced.  Returns what
+ * farn_forward would return before launching. */
+int farn_check_args(const void *const *partials, int W,
+                    const void *residual, const void *weight, float eps,
+                    int64_t T, int64_t H,
+                    const void *reduced_out, const void *residual_out,
+                    const void *norm_out);
+
+/* Release a context (NULL is accepted).  Returns FARN_OK. */
+int farn_destroy(farn_ctx *ctx);
+
+/* Text for a farn_status value (never NULL). */
+const char *farn_status_string(int status);
+
+/* Which kernel variant farn_forward would launch for this shape and these
+ * pointers, without launching: 0 row (one CTA per row), 1 cluster (a
+ * cluster of CTAs splits each row), 2 generic (any H or alignment).
+ * *cluster_size receives the CTAs per row (1 for row and generic),
+ * *threads the threads per CTA.  Returns a farn_status. */
+int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,
+              const void *const *partials, const void *residual,
+              const void *weight, const void *reduced_out,
+              const void *residual_out, const void *norm_out,
+              int *variant, int *cluster_size, int *threads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FARN_H_ */

@@ -1,0 +1,222 @@
+"""Fused rank-sum + residual add + RMSNorm for one GB300 (sm_103a).
+
+    reduced      = sum over ranks r of x[r]            (bf16 [T,H] each)
+    residual_out = reduced + residual
+    norm_out     = RMSNorm(residual_out, weight, eps)
+
+The operator of FlagTree pull request "[TLERaw] Add NVSHMEM allreduce
+RMSNorm tutorial" (Summary; Implementation sections 2-3), computed by the
+hand-written CUDA kernels of ``libfarn.so``.  This module is the Python
+binding of that library's C ABI (``include/farn.h``): the ``farn_*``
+functions have the C names and arguments and only marshal them through
+ctypes; ``forward`` is the same call for torch tensors.  Every arithmetic
+step runs in the CUDA kernels.  There is no CPU fallback: if the library
+is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build_library
+
+__all__ = [
+    "FARN_MAX_W", "FarnError", "Context", "build_library", "library_path",
+    "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
+    "farn_plan", "farn_status_string", "forward", "VARIANTS",
+]
+
+FARN_MAX_W = 32
+FARN_OK = 0
+FARN_ERR_INVALID_ARG = -1
+FARN_ERR_UNSUPPORTED = -2
+FARN_ERR_ALIAS = -3
+FARN_ERR_CUDA = -4
+FARN_ERR_NOMEM = -5
+VARIANTS = {0: "row", 1: "cluster", 2: "generic"}
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built (the operator has no CPU fallback); "
+                "run rank_sum_residual_gb300.build_library() on a machine with nvcc")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, cvp = ctypes.c_void_p, ctypes.c_void_p
+        pvp = ctypes.POINTER(ctypes.c_void_p)
+        i64, i32, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.farn_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        lib.farn_create.restype = i32
+        lib.farn_destroy.argtypes = [vp]
+        lib.farn_destroy.restype = i32
+        lib.farn_forward.argtypes = [vp, pvp, i32, cvp, cvp, f32, i64, i64,
+                                     vp, vp, vp, vp]
+        lib.farn_forward.restype = i32
+        lib.farn_check_args.argtypes = [pvp, i32, cvp, cvp, f32, i64, i64,
+                                        cvp, cvp, cvp]
+        lib.farn_check_args.restype = i32
+        lib.farn_plan.argtypes = [vp, i32, i64, i64, pvp, cvp, cvp, cvp, cvp,
+                                  cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                  ctypes.POINTER(i32)]
+        lib.farn_plan.restype = i32
+        lib.farn_status_string.argtypes = [i32]
+        lib.farn_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+class FarnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {farn_status_string(status)} (status {status})")
+
+
+def farn_status_string(status: int) -> str:
+    return _load().farn_status_string(int(status)).decode()
+
+
+def _ptr_array(ptrs):
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*[ctypes.c_void_p(int(p)) for p in ptrs])
+
+
+def farn_create(device: int = 0) -> int:
+    """C ``farn_create``: returns the opaque context handle (an int)."""
+    h = ctypes.c_void_p()
+    st = _load().farn_create(ctypes.byref(h), int(device))
+    if st != FARN_OK:
+        raise FarnError(st, "farn_create")
+    return h.value
+
+
+def farn_destroy(ctx: int) -> None:
+    _load().farn_destroy(ctypes.c_void_p(ctx) if ctx else None)
+
+
+def farn_forward(ctx, partials, W, residual, weight, eps, T, H,
+                 reduced_out, residual_out, norm_out, stream=0) -> int:
+    """C ``farn_forward`` on raw device addresses (ints); returns the status."""
+    return _load().farn_forward(
+        ctypes.c_void_p(ctx) if ctx else None, _ptr_array(partials), int(W),
+        ctypes.c_void_p(int(residual)), ctypes.c_void_p(int(weight)), float(eps),
+        int(T), int(H), ctypes.c_void_p(int(reduced_out)),
+        ctypes.c_void_p(int(residual_out)), ctypes.c_void_p(int(norm_out)),
+        ctypes.c_void_p(int(stream)))
+
+
+def farn_check_args(partials, W, residual, weight, eps, T, H, reduced_out,
+                    residual_out, norm_out) -> int:
+    """C ``farn_check_args``: host-only checks, addresses are only compared."""
+    arr = None if partials is None else _ptr_array(partials)
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    return _load().farn_check_args(arr, int(W), v(residual), v(weight),
+                                   float(eps), int(T), int(H), v(reduced_out),
+                                   v(residual_out), v(norm_out))
+
+
+def farn_plan(ctx, W, T, H, partials, residual, weight, reduced_out,
+              residual_out, norm_out):
+    """C ``farn_plan``: (variant name, CTAs per row, threads per CTA)."""
+    variant, cs, thr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    st = _load().farn_plan(ctypes.c_void_p(ctx), int(W), int(T), int(H),
+                           _ptr_array(partials), v(residual), v(weight),
+                           v(reduced_out), v(residual_out), v(norm_out),
+                           ctypes.byref(variant), ctypes.byref(cs),
+                           ctypes.byref(thr))
+    if st != FARN_OK:
+        raise FarnError(st, "farn_plan")
+    return VARIANTS[variant.value], cs.value, thr.value
+
+
+class Context:
+    """Owns one ``farn_ctx`` for a device (``farn_create``/``farn_destroy``)."""
+
+    def __init__(self, device: int = 0):
+        self.device = int(device)
+        self.handle = farn_create(self.device)
+
+    def close(self):
+        if self.handle:
+            farn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+_default_ctx: dict[int, Context] = {}
+
+
+def _context_for(device_index: int) -> Context:
+    c = _default_ctx.get(device_index)
+    if c is None:
+        c = _default_ctx[device_index] = Context(device_index)
+    return c
+
+
+def _check_tensor(t, name, shape, device):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def forward(partials, residual, weight, eps: float, out=None, ctx=None,
+            stream=None):
+    """The fused operator on torch bf16 CUDA tensors.
+
+    partials: sequence of W tensors [T,H]; residual [T,H]; weight [H].
+    out: optional (reduced, residual_out, norm_out) tensors to write
+    (residual_out may be ``residual`` itself).  Runs asynchronously on
+    ``stream`` (default: torch's current stream) and returns the outputs.
+    """
+    import torch
+    partials = list(partials)
+    if not partials:
+        raise ValueError("partials must hold at least one tensor")
+    if residual.dim() != 2:
+        raise ValueError("residual must be [T, H]")
+    T, H = residual.shape
+    dev = residual.device
+    for r, x in enumerate(partials):
+        _check_tensor(x, f"partials[{r}]", (T, H), dev)
+    _check_tensor(residual, "residual", (T, H), dev)
+    _check_tensor(weight, "weight", (H,), dev)
+    if out is None:
+        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+                    for _ in range(3))
+    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
+        _check_tensor(t, name, (T, H), dev)
+    c = ctx if ctx is not None else _context_for(dev.index)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = farn_forward(c.handle, [x.data_ptr() for x in partials], len(partials),
+                      residual.data_ptr(), weight.data_ptr(), eps, T, H,
+                      out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+                      s.cuda_stream)
+    if st != FARN_OK:
+        raise FarnError(st, "farn_forward")
+    return out

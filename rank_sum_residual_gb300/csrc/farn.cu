@@ -1,0 +1,360 @@
+// Host side of libfarn.so: the C ABI declared in include/farn.h.
+//
+// Argument checks, the choice of kernel variant for a shape, and the launch
+// on the caller's stream.  The page's host side (FlagTree pull request
+// "[TLERaw] Add NVSHMEM allreduce RMSNorm tutorial", Implementation
+// section 4) initialises NVSHMEM, bootstraps the ranks and manages a
+// symmetric workspace behind a host C ABI; on one GPU none of that exists,
+// so the context only caches device properties and kernel attributes, and
+// the library allocates no device memory at all.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "farn.h"
+#include "farn_kernels.cuh"
+
+static_assert(FARN_MAX_W == farn::kMaxW, "FARN_MAX_W and kernel limit differ");
+
+enum { kVariantRow = 0, kVariantCluster = 1, kVariantGeneric = 2, kVariantAuto = -1 };
+
+struct farn_ctx {
+  int device;
+  int num_sms;
+  int max_cluster;     // largest power-of-two cluster size that can be scheduled
+  int force_variant;   // kVariantAuto unless FARN_VARIANT says otherwise
+  int force_cluster;   // 0 = choose; else CTAs per row for the cluster variant
+  int force_vpt;       // 0 = choose; else 16-byte vectors per thread
+};
+
+namespace {
+
+struct Plan {
+  int variant;
+  int cs;       // CTAs per row
+  int vpt;      // vectors per thread
+  int threads;  // threads per CTA
+  int64_t grid;
+};
+
+typedef void (*VecKernel)(const farn::Params);
+
+template <int VPT, int CS>
+VecKernel vec_kernel() { return &farn::farn_vec_kernel<VPT, CS>; }
+
+VecKernel pick_vec(int vpt, int cs) {
+  switch (cs) {
+    case 1:
+      switch (vpt) { case 1: return vec_kernel<1, 1>(); case 2: return vec_kernel<2, 1>();
+                     case 4: return vec_kernel<4, 1>(); }
+      break;
+    case 2:
+      switch (vpt) { case 1: return vec_kernel<1, 2>(); case 2: return vec_kernel<2, 2>();
+                     case 4: return vec_kernel<4, 2>(); }
+      break;
+    case 4:
+      switch (vpt) { case 1: return vec_kernel<1, 4>(); case 2: return vec_kernel<2, 4>();
+                     case 4: return vec_kernel<4, 4>(); }
+      break;
+    case 8:
+      switch (vpt) { case 1: return vec_kernel<1, 8>(); case 2: return vec_kernel<2, 8>();
+                     case 4: return vec_kernel<4, 8>(); }
+      break;
+    case 16:
+      switch (vpt) { case 1: return vec_kernel<1, 16>(); case 2: return vec_kernel<2, 16>();
+                     case 4: return vec_kernel<4, 16>(); }
+      break;
+  }
+  return nullptr;
+}
+
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  if (na <= 0 || nb <= 0) return false;
+  uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + (uintptr_t)nb && b0 < a0 + (uintptr_t)na;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int env_int(const char* name, int dflt) {
+  const char* s = getenv(name);
+  if (!s || !*s) return dflt;
+  return atoi(s);
+}
+
+// Vectors per thread for a slice of sv 16-byte vectors (the vector kernel
+// takes at most 512 threads, so slices of up to 2048 vectors, H <= 16384
+// for one CTA per row).
+int choose_vpt(int64_t sv) {
+  if (sv >= 512) return 4;
+  if (sv >= 128) return 2;
+  return 1;
+}
+
+int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
+  Plan pl;
+  const int64_t hv = H / 8;
+  int want = ctx->force_variant;
+  if (!vec_ok || want == kVariantGeneric) {
+    pl.variant = kVariantGeneric;
+    pl.cs = 1; pl.vpt = 1; pl.threads = 256;
+    pl.grid = T;
+  } else {
+    int cs = 1;
+    if (want == kVariantCluster || want == kVariantAuto) {
+      if (ctx->force_cluster > 0) {
+        cs = ctx->force_cluster;
+      } else {
+        // Smallest power of two that puts about one CTA on every SM,
+        // while each CTA keeps at least one warp of 16-byte vectors.
+        const int cap = ctx->max_cluster;
+        while (T * cs < ctx->num_sms && cs * 2 <= cap && hv % (cs * 2) == 0 &&
+               hv / (cs * 2) >= 32)
+          cs *= 2;
+        if (want == kVariantCluster && cs == 1 && cap >= 2 && hv % 2 == 0) cs = 2;
+      }
+      if (cs > ctx->max_cluster || hv % cs != 0) return FARN_ERR_UNSUPPORTED;
+    }
+    const int64_t sv = hv / cs;
+    int vpt = ctx->force_vpt > 0 ? ctx->force_vpt : choose_vpt(sv);
+    int64_t threads = (sv + vpt - 1) / vpt;
+    threads = (threads + 31) / 32 * 32;
+    if (threads > 512) {
+      // Too long for one CTA's registers: the generic kernel takes it.
+      pl.variant = kVariantGeneric;
+      pl.cs = 1; pl.vpt = 1; pl.threads = 256; pl.grid = T;
+      *out = pl;
+      return FARN_OK;
+    }
+    if (!pick_vec(vpt, cs)) return FARN_ERR_UNSUPPORTED;
+    pl.variant = cs > 1 ? kVariantCluster : kVariantRow;
+    pl.cs = cs; pl.vpt = vpt; pl.threads = (int)threads;
+    pl.grid = T * cs;
+  }
+  // Grid limit: rows beyond one pass are looped over inside the kernel.
+  const int64_t max_grid = (int64_t)0x7FFFFFFF / pl.cs * pl.cs;
+  if (pl.grid > max_grid) pl.grid = max_grid;
+  *out = pl;
+  return FARN_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* farn_status_string(int status) {
+  switch (status) {
+    case FARN_OK: return "ok";
+    case FARN_ERR_INVALID_ARG: return "invalid argument";
+    case FARN_ERR_UNSUPPORTED: return "unsupported shape or launch configuration";
+    case FARN_ERR_ALIAS: return "an output overlaps an input or another output";
+    case FARN_ERR_CUDA: return "CUDA runtime error";
+    case FARN_ERR_NOMEM: return "out of host memory";
+  }
+  return "unknown status";
+}
+
+int farn_check_args(const void* const* partials, int W, const void* residual,
+                    const void* weight, float eps, int64_t T, int64_t H,
+                    const void* reduced_out, const void* residual_out,
+                    const void* norm_out) {
+  if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1) return FARN_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
+  if (!residual || !weight || !reduced_out || !residual_out || !norm_out)
+    return FARN_ERR_INVALID_ARG;
+  for (int r = 0; r < W; ++r)
+    if (!partials[r]) return FARN_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 2 || (T > 0 && T > INT64_MAX / (2 * H))) return FARN_ERR_INVALID_ARG;
+  const int64_t nb = T * H * 2, wb = H * 2;
+  const void* outs[3] = {reduced_out, residual_out, norm_out};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], nb, outs[j], nb)) return FARN_ERR_ALIAS;
+    for (int r = 0; r < W; ++r)
+      if (overlaps(outs[i], nb, partials[r], nb)) return FARN_ERR_ALIAS;
+    if (overlaps(outs[i], nb, weight, wb)) return FARN_ERR_ALIAS;
+    const bool inplace_residual = (i == 1 && residual_out == residual);
+    if (!inplace_residual && overlaps(outs[i], nb, residual, nb)) return FARN_ERR_ALIAS;
+  }
+  return FARN_OK;
+}
+
+int farn_create(farn_ctx** out, int device) {
+  if (!out || device < 0) return FARN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "create") == 0)
+    return FARN_ERR_CUDA;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  if (device >= ndev) return FARN_ERR_INVALID_ARG;
+  DeviceGuard g(device);
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+
+  farn_ctx* c = new (std::nothrow) farn_ctx;
+  if (!c) return FARN_ERR_NOMEM;
+  c->device = device;
+  if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete c;
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  // Cluster sizes up to 8 are portable; 16 needs the non-portable opt-in
+  // and must still fit on a GPC, which the occupancy query answers.
+  c->max_cluster = 8;
+  {
+    VecKernel k16 = pick_vec(1, 16);
+    if (cudaFuncSetAttribute((const void*)k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      bool ok16 = true;
+      for (int vpt = 1; vpt <= 4; vpt *= 2) {
+        VecKernel k = pick_vec(vpt, 16);
+        if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) { ok16 = false; break; }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 16; attr.val.clusterDim.y = 1; attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, (const void*)k, &cfg) != cudaSuccess ||
+            nclusters < 1) { ok16 = false; break; }
+      }
+      if (ok16) c->max_cluster = 16;
+    }
+    cudaGetLastError();
+  }
+  c->force_variant = kVariantAuto;
+  if (const char* v = getenv("FARN_VARIANT")) {
+    if (!strcmp(v, "row")) c->force_variant = kVariantRow;
+    else if (!strcmp(v, "cluster")) c->force_variant = kVariantCluster;
+    else if (!strcmp(v, "generic")) c->force_variant = kVariantGeneric;
+  }
+  c->force_cluster = env_int("FARN_CLUSTER", 0);
+  if (c->force_cluster != 0 && c->force_cluster != 1 && c->force_cluster != 2 &&
+      c->force_cluster != 4 && c->force_cluster != 8 && c->force_cluster != 16)
+    c->force_cluster = 0;
+  c->force_vpt = env_int("FARN_VPT", 0);
+  if (c->force_vpt != 0 && c->force_vpt != 1 && c->force_vpt != 2 && c->force_vpt != 4)
+    c->force_vpt = 0;
+  *out = c;
+  return FARN_OK;
+}
+
+int farn_destroy(farn_ctx* ctx) {
+  delete ctx;
+  return FARN_OK;
+}
+
+static bool vector_path_ok(int W, const void* const* partials, const void* residual,
+                           const void* weight, const void* reduced_out,
+                           const void* residual_out, const void* norm_out, int64_t H) {
+  if (H % 8 != 0) return false;
+  for (int r = 0; r < W; ++r)
+    if (!aligned16(partials[r])) return false;
+  return aligned16(residual) && aligned16(weight) && aligned16(reduced_out) &&
+         aligned16(residual_out) && aligned16(norm_out);
+}
+
+int farn_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, const void* const* partials,
+              const void* residual, const void* weight, const void* reduced_out,
+              const void* residual_out, const void* norm_out, int* variant,
+              int* cluster_size, int* threads) {
+  if (!ctx || !variant || !cluster_size || !threads) return FARN_ERR_INVALID_ARG;
+  int st = farn_check_args(partials, W, residual, weight, 1.0f, T, H, reduced_out,
+                           residual_out, norm_out);
+  if (st != FARN_OK) return st;
+  Plan pl;
+  st = make_plan(ctx, T, H,
+                 vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
+                                norm_out, H),
+                 &pl);
+  if (st != FARN_OK) return st;
+  *variant = pl.variant;
+  *cluster_size = pl.cs;
+  *threads = pl.threads;
+  return FARN_OK;
+}
+
+int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
+                 const void* residual, const void* weight, float eps, int64_t T,
+                 int64_t H, void* reduced_out, void* residual_out, void* norm_out,
+                 cudaStream_t stream) {
+  if (!ctx) return FARN_ERR_INVALID_ARG;
+  int st = farn_check_args(partials, W, residual, weight, eps, T, H, reduced_out,
+                           residual_out, norm_out);
+  if (st != FARN_OK) return st;
+  if (T == 0) return FARN_OK;
+  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
+    return FARN_ERR_CUDA;
+
+  Plan pl;
+  st = make_plan(ctx, T, H,
+                 vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
+                                norm_out, H),
+                 &pl);
+  if (st != FARN_OK) return st;
+
+  farn::Params prm;
+  memset(&prm, 0, sizeof prm);
+  for (int r = 0; r < W; ++r) prm.x[r] = partials[r];
+  prm.residual = residual;
+  prm.weight = weight;
+  prm.reduced = reduced_out;
+  prm.residual_out = residual_out;
+  prm.norm_out = norm_out;
+  prm.T = T;
+  prm.H = H;
+  prm.W = W;
+  prm.eps = eps;
+
+  DeviceGuard g(ctx->device);
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)pl.cs;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = pl.cs > 1 ? 1 : 0;
+
+  cudaError_t err;
+  if (pl.variant == kVariantGeneric) {
+    err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel, prm);
+  } else {
+    VecKernel k = pick_vec(pl.vpt, pl.cs);
+    err = cudaLaunchKernelEx(&cfg, k, prm);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  return FARN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,333 @@
+// Device code of the fused rank-sum + residual add + RMSNorm operator for
+// sm_103a (GB300).
+//
+// Operation: FlagTree pull request "[TLERaw] Add NVSHMEM allreduce RMSNorm
+// tutorial", Summary (reduced = sum of the rank partials, residual_out =
+// reduced + residual, norm_out = RMSNorm(residual_out, weight, eps)) and
+// Implementation section 3 (the residual + RMSNorm epilogue with FP32
+// accumulation), fused into one pass over HBM.
+//
+// The page maps one token row to one CTA (Implementation section 2).  That
+// mapping is kept for long inputs (CS == 1).  For decode-sized T, where one
+// CTA per row would leave most of the 152 SMs idle, a thread-block cluster
+// of CS CTAs splits each row; the CTAs of a cluster exchange their partial
+// sums of squares through distributed shared memory (DSMEM).
+//
+// Per element the arithmetic is fixed (f = exact bf16 -> fp32 widening,
+// bf16 = round to nearest even):
+//   acc = -0.0f; for r in 0..W-1: acc += f(x[r])      // -0 is the exact
+//   red = bf16(acc)                                    // additive identity,
+//   ro  = bf16(f(red) + f(residual))                   // so acc == f(x[0])
+//   ss += f(ro)^2                                      // after rank 0
+//   norm = bf16((f(ro) * rstd) * f(weight)),  rstd = 1/sqrt(ss/H + eps)
+// so `reduced` and `residual_out` do not depend on the launch shape; only
+// the order of the row's sum of squares does.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace farn {
+
+constexpr int kMaxW = 32;
+
+// Kernel parameters, passed by value (__grid_constant__): the W partial
+// pointers are indexed by rank straight from the parameter bank.
+struct Params {
+  const void* x[kMaxW];
+  const void* residual;
+  const void* weight;
+  void* reduced;
+  void* residual_out;
+  void* norm_out;
+  int64_t T;     // rows
+  int64_t H;     // elements per row
+  int W;         // partials
+  float eps;
+};
+
+// ----------------------------------------------------------- bf16 helpers
+// The two bf16 values of a 32-bit word: element 2e is the low half.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round two fp32 values to bf16 (nearest even) and pack them, lo in the
+// low half.  One cvt.rn.bf16x2.f32 instruction.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float v) {
+  return (uint16_t)(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+}
+
+// ----------------------------------------------------------- memory access
+// Partials: read once, never written by this kernel -> non-coherent path,
+// no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// Residual: coherent load (residual_out may be the same buffer; every
+// element is read before the same thread overwrites it).
+__device__ __forceinline__ uint4 ld_coherent(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// Weight: shared by every row, keep it cached.
+__device__ __forceinline__ uint4 ld_keep(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+// Outputs: written once, streamed out (evict-first).
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void add8(float* acc, uint4 v) {
+  acc[0] += bf_lo(v.x); acc[1] += bf_hi(v.x);
+  acc[2] += bf_lo(v.y); acc[3] += bf_hi(v.y);
+  acc[4] += bf_lo(v.z); acc[5] += bf_hi(v.z);
+  acc[6] += bf_lo(v.w); acc[7] += bf_hi(v.w);
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Read a float from the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// --------------------------------------------------------- vector kernel
+// Each CTA owns the column slice `slice` (of CS) of one row; each thread
+// owns VPT 16-byte vectors (8 bf16 each) of that slice, at
+// j = threadIdx.x + k*blockDim.x.  The slice is sv = H/8/CS vectors; the
+// host guarantees H % 8 == 0, (H/8) % CS == 0, 16-byte aligned pointers and
+// blockDim.x * VPT >= sv.
+//
+// Partials are loaded G ranks at a time (G*VPT = 8 vectors in flight per
+// thread per batch, plus the residual of the first batch) and added in
+// rank order.  At most 512 threads per CTA (128 registers per thread).
+template <int VPT, int CS>
+__global__ void __launch_bounds__(512)
+farn_vec_kernel(const __grid_constant__ Params p) {
+  constexpr int G = (8 / VPT) > 0 ? (8 / VPT) : 1;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const int64_t hv = p.H >> 3;
+  const int sv = (int)(hv / CS);
+  const uint32_t slice = (CS == 1) ? 0u : cluster_ctarank();
+  const float Hf = (float)p.H;
+
+  __shared__ float warp_ss[2][32];
+  __shared__ float cta_ss;
+
+  const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
+
+  const int64_t rows_per_pass = gridDim.x / CS;
+  int it = 0;
+  for (int64_t row = blockIdx.x / CS; row < p.T; row += rows_per_pass, ++it) {
+    const int64_t base = row * hv + (int64_t)slice * sv;   // vector offset
+
+    uint4 rv[VPT];
+    float acc[VPT][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) rv[k] = ld_coherent(reinterpret_cast<const uint4*>(p.residual) + base + j);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
+    }
+
+    // a1: rank sum in fp32, rank order 0..W-1.
+    for (int r0 = 0; r0 < p.W; r0 += G) {
+      uint4 xv[G][VPT];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int r = r0 + g;
+        const uint4* xp = reinterpret_cast<const uint4*>(p.x[r < p.W ? r : 0]) + base;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int j = tid + k * blockDim.x;
+          xv[g][k] = make_uint4(0u, 0u, 0u, 0u);
+          if (r < p.W && j < sv) xv[g][k] = ld_stream(xp + j);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (r0 + g < p.W) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) add8(acc[k], xv[g][k]);
+        }
+      }
+    }
+
+    // a2 + a5: reduced and residual_out, rounded and stored; a3: the
+    // thread's part of the sum of squares of the rounded residual_out.
+    uint4 ro[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) {
+        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        uint32_t red[4], out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
+          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+          out[e] = pack_bf16x2(s0, s1);
+          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+          ss = fmaf(q0, q0, ss);
+          ss = fmaf(q1, q1, ss);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                  make_uint4(red[0], red[1], red[2], red[3]));
+        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+      }
+    }
+
+    // The weight slice (cached: every row reads it) is fetched here so its
+    // latency hides behind the reduction below and it holds no registers
+    // during the rank loop.
+    uint4 wv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) wv[k] = ld_keep(wv4 + j);
+    }
+
+    // a3: CTA sum of squares (warp butterfly, then the warps' sums in
+    // warp order; every thread forms the same total).
+    ss = warp_sum(ss);
+    float* ws = warp_ss[it & 1];
+    if (lane == 0) ws[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += ws[w];
+
+    if (CS > 1) {
+      // Cluster: the CTAs' totals through DSMEM, summed in CTA-rank order
+      // by every warp (lane c fetches CTA c's total).
+      if (tid == 0) cta_ss = tot;
+      cluster_arrive_release();
+      cluster_wait_acquire();
+      float mine = 0.0f;
+      if (lane < CS) mine = ld_dsmem_f32(&cta_ss, (uint32_t)lane);
+      tot = 0.0f;
+#pragma unroll
+      for (int c = 0; c < CS; ++c) tot += __shfl_sync(0xFFFFFFFFu, mine, c);
+      // Every thread has read what it needs from its peers; the matching
+      // wait below keeps each CTA's shared memory alive (and cta_ss
+      // unchanged) until all peers are done with it.
+      cluster_arrive_relaxed();
+    }
+
+    // a4: rstd with IEEE division and square root, then the normalised,
+    // weighted output.
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) {
+        const uint32_t q[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
+        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint32_t n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n0 = (bf_lo(q[e]) * rstd) * bf_lo(w[e]);
+          const float n1 = (bf_hi(q[e]) * rstd) * bf_hi(w[e]);
+          n[e] = pack_bf16x2(n0, n1);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                  make_uint4(n[0], n[1], n[2], n[3]));
+      }
+    }
+    if (CS > 1) cluster_wait_acquire();
+  }
+}
+
+// -------------------------------------------------------- generic kernel
+// Any H, any alignment: one CTA per row, scalar bf16 accesses, two passes
+// (the second re-reads the residual_out this same thread wrote).
+__global__ void __launch_bounds__(256)
+farn_generic_kernel(const __grid_constant__ Params p) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const float Hf = (float)p.H;
+  __shared__ float warp_ss[2][32];
+  const uint16_t* res = reinterpret_cast<const uint16_t*>(p.residual);
+  const uint16_t* wt = reinterpret_cast<const uint16_t*>(p.weight);
+  uint16_t* red_out = reinterpret_cast<uint16_t*>(p.reduced);
+  uint16_t* ro_out = reinterpret_cast<uint16_t*>(p.residual_out);
+  uint16_t* nrm_out = reinterpret_cast<uint16_t*>(p.norm_out);
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+    const int64_t off = row * p.H;
+    float ss = 0.0f;
+    for (int64_t h = tid; h < p.H; h += blockDim.x) {
+      float acc = -0.0f;
+      for (int r = 0; r < p.W; ++r)
+        acc += __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p.x[r])[off + h] << 16);
+      const uint16_t rb = to_bf16(acc);
+      red_out[off + h] = rb;
+      const float s = __uint_as_float((uint32_t)rb << 16) +
+                      __uint_as_float((uint32_t)res[off + h] << 16);
+      const uint16_t ob = to_bf16(s);
+      ro_out[off + h] = ob;
+      const float q = __uint_as_float((uint32_t)ob << 16);
+      ss = fmaf(q, q, ss);
+    }
+    ss = warp_sum(ss);
+    float* ws = warp_ss[it & 1];
+    if (lane == 0) ws[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += ws[w];
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+    for (int64_t h = tid; h < p.H; h += blockDim.x) {
+      const float q = __uint_as_float((uint32_t)ro_out[off + h] << 16);
+      const float w = __uint_as_float((uint32_t)wt[h] << 16);
+      nrm_out[off + h] = to_bf16((q * rstd) * w);
+    }
+  }
+}
+
+}  // namespace farn

@@ -1,0 +1,141 @@
+"""The C ABI on the host (no GPU needed): the library loads, exports every
+function include/farn.h declares, and its argument checks return the
+documented status without touching the pointers."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rank_sum_residual_gb300 as farn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "farn.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    farn.build_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(farn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("farn_create", "farn_forward", "farn_destroy", "farn_check_args",
+              "farn_status_string", "farn_plan"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(farn.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libfarn.so does not export {name}"
+
+
+def test_status_strings():
+    assert farn.farn_status_string(0) == "ok"
+    for st in (-1, -2, -3, -4, -5):
+        assert farn.farn_status_string(st) not in ("", "unknown status")
+    assert farn.farn_status_string(12345) == "unknown status"
+
+
+# Fake, never-dereferenced addresses: 1 MiB apart, 16-byte aligned.
+MB = 1 << 20
+X = [0x10000000 + i * MB for i in range(40)]
+RES, WT, RED, RO, NRM = 0x20000000, 0x21000000, 0x22000000, 0x23000000, 0x24000000
+
+
+def check(partials=None, W=None, residual=RES, weight=WT, eps=1e-6, T=4, H=64,
+          red=RED, ro=RO, nrm=NRM):
+    partials = X[:4] if partials is None else partials
+    W = len(partials) if W is None else W
+    return farn.farn_check_args(partials, W, residual, weight, eps, T, H, red, ro, nrm)
+
+
+def test_valid_arguments_pass():
+    assert check() == 0
+    assert check(T=0) == 0
+    assert check(partials=X[:32]) == 0
+    assert check(partials=X[:1]) == 0
+    # residual_out may be exactly the residual buffer (in-place update)
+    assert check(ro=RES) == 0
+    # partials may repeat (read-only inputs may overlap)
+    assert check(partials=[X[0], X[0], X[1]]) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(W=0, partials=X[:1]), dict(partials=X[:33]), dict(T=-1), dict(H=0),
+    dict(H=-8), dict(eps=-1e-6), dict(eps=float("nan")), dict(eps=float("inf")),
+    dict(residual=0), dict(weight=0), dict(red=0), dict(ro=0), dict(nrm=0),
+    dict(partials=[X[0], 0, X[1]]), dict(H=1 << 62, T=4),
+])
+def test_invalid_arguments(kw):
+    assert check(**kw) == farn.FARN_ERR_INVALID_ARG
+
+
+def test_null_partials_array():
+    assert farn.farn_check_args(None, 2, RES, WT, 1e-6, 4, 64, RED, RO, NRM) \
+        == farn.FARN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(red=RO),                          # two outputs the same
+    dict(red=RO + 2 * 4 * 64 - 2),         # outputs overlap by one element
+    dict(nrm=X[2] + 16),                   # output inside a partial
+    dict(red=WT),                          # output over the weight
+    dict(nrm=RES),                         # only residual_out may alias residual
+    dict(ro=RES + 16),                     # residual_out partially over residual
+])
+def test_aliasing_rejected(kw):
+    assert check(**kw) == farn.FARN_ERR_ALIAS
+
+
+def test_adjacent_buffers_are_not_aliases():
+    nb = 4 * 64 * 2
+    assert check(red=RED, ro=RED + nb, nrm=RED + 2 * nb) == 0
+
+
+def test_forward_rejects_null_context_before_any_cuda_call():
+    st = farn.farn_forward(0, X[:4], 4, RES, WT, 1e-6, 4, 64, RED, RO, NRM, 0)
+    assert st == farn.FARN_ERR_INVALID_ARG
+
+
+def test_create_without_a_gpu_reports_cuda_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; the GPU tests cover farn_create")
+    with pytest.raises(farn.FarnError) as e:
+        farn.farn_create(0)
+    assert e.value.status in (farn.FARN_ERR_CUDA, farn.FARN_ERR_INVALID_ARG)
+    with pytest.raises(farn.FarnError) as e:
+        farn.farn_create(-1)
+    assert e.value.status == farn.FARN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import importlib
+    import rank_sum_residual_gb300 as pkg
+    monkeypatch.setattr(pkg, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(pkg, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pkg.farn_status_string(0)
+    importlib.reload(pkg)
+
+
+def test_synth_twin_recipe_statistics():
+    import numpy as np
+    import synth
+    p = synth.workload("wide")[0]
+    xs, res, w = synth.host_inputs(p.with_T(64))
+    x = (xs[0].astype(np.uint32) << 16).view(np.float32)
+    assert abs(x.var() - 1.0 / 16) < 0.005          # N(0, 1/16): variance
+    r = (res.astype(np.uint32) << 16).view(np.float32)
+    assert abs(r.mean()) < 0.02 and abs(r.var() - 1.0) < 0.05
+    # different streams differ, same stream repeats
+    assert not np.array_equal(xs[0], xs[1])
+    assert np.array_equal(synth.host_bf16(1000, 0, 3, p.x), synth.host_bf16(1000, 0, 3, p.x))

@@ -1,0 +1,341 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU
+oracle on the same seeded device-generated inputs.
+
+reduced and residual_out must match bit for bit, norm_out within one bf16
+ulp (tests/parity.py).  Covers the five benchmark shapes (full size on
+sampled rows, and mid-size shapes spanning many CTAs with a ragged row
+count in full), every kernel variant, and the edge cases: empty and
+one-row inputs, odd H, misaligned pointers, W = 1 and W = 32, zero rows,
+NaN and overflow, in-place residual, guard regions around the outputs,
+argument errors and injected launch faults.
+"""
+import os
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle  # noqa: E402
+import rank_sum_residual_gb300 as farn  # noqa: E402
+import synth  # noqa: E402
+from parity import assert_parity, compare, sample_rows, u16  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x7BAD          # a finite bf16 pattern no output of these tests has
+
+
+@pytest.fixture(scope="session")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    farn.build_library()
+    synth.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.fixture(scope="session")
+def O():
+    return oracle.Oracle()
+
+
+def make_ctx(**env):
+    """A context created under the given FARN_* environment (read at create)."""
+    old = {k: os.environ.get(k) for k in env}
+    try:
+        for k, v in env.items():
+            os.environ[k] = str(v)
+        return farn.Context(0)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def oracle_rows(O, xs, res, w, eps, rows=None):
+    if rows is None:
+        return O.forward([u16(x) for x in xs], u16(res), u16(w), eps)
+    idx = torch.as_tensor(rows, device=res.device)
+    return O.forward([u16(x.index_select(0, idx)) for x in xs],
+                     u16(res.index_select(0, idx)), u16(w), eps)
+
+
+def run_and_check(O, p, dev, ctx=None, rows=None, what=""):
+    xs, res, w = synth.device_inputs(p, dev)
+    out = farn.forward(xs, res, w, p.eps, ctx=ctx)
+    torch.cuda.synchronize()
+    want = oracle_rows(O, xs, res, w, p.eps, rows)
+    if rows is None:
+        got = [u16(t) for t in out]
+    else:
+        idx = torch.as_tensor(rows, device=dev)
+        got = [u16(t.index_select(0, idx)) for t in out]
+    return assert_parity(got, want, what or p.name)
+
+
+# ------------------------------------------------------------ the workloads
+def test_c1_full(O, dev):
+    run_and_check(O, synth.workload("c1")[0], dev)
+
+
+@pytest.mark.parametrize("T", synth.DECODE_TS)
+def test_decode_sweep_full(O, dev, T):
+    p = [q for q in synth.workload("decode") if q.T == T][0]
+    run_and_check(O, p, dev)
+
+
+@pytest.mark.parametrize("name,T", [("prefill", 333), ("nonpow2", 517), ("wide", 257),
+                                    ("prefill", 1), ("wide", 9)])
+def test_mid_size_full(O, dev, name, T):
+    """The large shapes' H, W and value recipes at a row count the oracle
+    finishes in seconds, ragged against every grid size."""
+    run_and_check(O, synth.workload(name)[0].with_T(T), dev)
+
+
+@pytest.mark.parametrize("name", ["prefill", "nonpow2", "wide"])
+def test_full_size_sampled_rows(O, dev, name):
+    """Full benchmark size, default launch plan (as the benchmark times it);
+    the oracle recomputes 160 sampled rows (first, middle, last, random)."""
+    p = synth.workload(name)[0]
+    rows = sample_rows(p.T, 160, seed=p.W)
+    run_and_check(O, p, dev, rows=rows)
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- variants
+def _variant_outputs(dev, p, ctx):
+    xs, res, w = synth.device_inputs(p, dev)
+    out = farn.forward(xs, res, w, p.eps, ctx=ctx)
+    torch.cuda.synchronize()
+    return xs, res, w, [u16(t) for t in out]
+
+
+@pytest.mark.parametrize("env", [
+    dict(FARN_VARIANT="row"), dict(FARN_VARIANT="generic"),
+    dict(FARN_VARIANT="cluster", FARN_CLUSTER=2), dict(FARN_VARIANT="cluster", FARN_CLUSTER=4),
+    dict(FARN_VARIANT="cluster", FARN_CLUSTER=8), dict(FARN_VARIANT="cluster", FARN_CLUSTER=16),
+    dict(FARN_VARIANT="row", FARN_VPT=1), dict(FARN_VARIANT="row", FARN_VPT=2),
+    dict(FARN_VARIANT="row", FARN_VPT=4),
+], ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
+@pytest.mark.parametrize("shape", [(8, 5, 4096), (4, 37, 5120), (16, 3, 7168)],
+                         ids=lambda s: f"W{s[0]}T{s[1]}H{s[2]}")
+def test_forced_variants_match_oracle_and_each_other(O, dev, env, shape):
+    W, T, H = shape
+    p = synth.Problem("variant", W, T, H, 1e-6, 17, synth.N01)
+    ctx = make_ctx(**env)
+    try:
+        xs, res, w, got = _variant_outputs(dev, p, ctx)
+        want = oracle_rows(O, xs, res, w, p.eps)
+        assert_parity(got, want, f"{env} {shape}")
+        # the default plan on the same input: reduced/residual_out identical
+        _, _, _, ref = _variant_outputs(dev, p, None)
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+        assert compare(got, ref)["norm_out"]["max_ulp"] <= 1
+    finally:
+        ctx.close()
+
+
+def test_plan_choices(dev):
+    c = farn.Context(0)
+    try:
+        def plan(W, T, H, off=0):
+            a = 0x10000000 + off
+            return farn.farn_plan(c.handle, W, T, H, [a] * W, a + 0x1000000,
+                                  a + 0x2000000, a + 0x3000000, a + 0x4000000, a + 0x5000000)
+        assert plan(8, 8192, 8192)[0] == "row"
+        assert plan(8, 1, 4096)[0] == "cluster"
+        assert plan(8, 1, 4096)[1] >= 8
+        assert plan(4, 16, 13)[0] == "generic"          # H % 8 != 0
+        assert plan(4, 16, 2048, off=2)[0] == "generic"  # misaligned
+        assert plan(4, 16, 32768)[0] == "generic"       # longer than one CTA
+    finally:
+        c.close()
+
+
+def test_deterministic(dev):
+    p = synth.workload("decode")[-1]
+    a = _variant_outputs(dev, p, None)[3]
+    b = _variant_outputs(dev, p, None)[3]
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+# ------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("W", [1, 2, 3, 16, 32])
+@pytest.mark.parametrize("T,H", [(1, 8), (3, 4), (3, 13), (2, 2048), (3, 5120),
+                                 (5, 8192), (2, 16384), (2, 16392), (1, 24576)])
+def test_edge_shapes(O, dev, W, T, H):
+    p = synth.Problem("edge", W, T, H, 1e-6, 5, synth.N01)
+    run_and_check(O, p, dev, what=f"W={W} T={T} H={H}")
+
+
+def test_empty_rows(dev):
+    xs = [torch.empty((0, 64), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    res = torch.empty((0, 64), dtype=torch.bfloat16, device=dev)
+    w = torch.ones(64, dtype=torch.bfloat16, device=dev)
+    out = farn.forward(xs, res, w, 1e-6)
+    torch.cuda.synchronize()
+    assert all(t.shape == (0, 64) for t in out)
+
+
+def _inputs(dev, W, T, H, seed=3):
+    p = synth.Problem("x", W, T, H, 1e-6, seed, synth.N01)
+    return synth.device_inputs(p, dev)
+
+
+def test_misaligned_pointers_take_generic_path(O, dev):
+    W, T, H = 3, 7, 2048
+    xs0, res0, w0 = _inputs(dev, W, T, H)
+    def shifted(t):                      # same values, 2-byte-offset storage
+        buf = torch.empty(t.numel() + 1, dtype=torch.bfloat16, device=dev)
+        v = buf[1:].view(t.shape)
+        v.copy_(t)
+        return v
+    xs = [shifted(x) for x in xs0]
+    res, w = shifted(res0), shifted(w0)
+    assert xs[0].data_ptr() % 16 == 2
+    outs = [shifted(torch.zeros((T, H), dtype=torch.bfloat16, device=dev)) for _ in range(3)]
+    c = farn._context_for(0)
+    assert farn.farn_plan(c.handle, W, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                          w.data_ptr(), *[o.data_ptr() for o in outs])[0] == "generic"
+    farn.forward(xs, res, w, 1e-6, out=outs)
+    torch.cuda.synchronize()
+    assert_parity([u16(o) for o in outs], oracle_rows(O, xs0, res0, w0, 1e-6), "misaligned")
+
+
+def test_special_values(O, dev):
+    """A zero row, a NaN in one partial, an overflowing sum, subnormals."""
+    W, T, H = 4, 6, 4096
+    xs, res, w = _inputs(dev, W, T, H)
+    for x in xs:
+        x[0].zero_()
+    res[0].zero_()
+    xs[2][1, 77] = float("nan")
+    big = torch.tensor(3.0e38, dtype=torch.bfloat16)
+    for x in xs:
+        x[2, 5] = big
+    tiny = torch.tensor([1]).to(torch.int16).view(torch.bfloat16)   # 2^-133
+    for x in xs:
+        x[3].view(torch.int16)[:] = 1
+    res[3].zero_()
+    out = farn.forward(xs, res, w, 1e-6)
+    torch.cuda.synchronize()
+    got = [u16(t) for t in out]
+    want = oracle_rows(O, xs, res, w, 1e-6)
+    assert_parity(got, want, "special values")
+    assert np.all(got[0][0] == 0) and np.all(got[2][0] == 0)
+    assert np.isnan(out[2][1].float().cpu().numpy()).all()
+    assert got[0][2, 5] == 0x7F80                     # +inf
+    assert np.all(got[0][3] == 4)                     # 4 * 2^-133, kept, not flushed
+    del tiny
+
+
+def test_in_place_residual(O, dev):
+    W, T, H = 8, 40, 4096
+    xs, res, w = _inputs(dev, W, T, H)
+    want = oracle_rows(O, xs, res, w, 1e-6)
+    red = torch.empty_like(res)
+    nrm = torch.empty_like(res)
+    farn.forward(xs, res, w, 1e-6, out=(red, res, nrm))
+    torch.cuda.synchronize()
+    assert_parity([u16(red), u16(res), u16(nrm)], want, "in-place residual")
+
+
+def test_guard_regions_untouched(O, dev):
+    """Outputs carved out of larger buffers: the guard words around them
+    must keep their sentinel (stands in for a memory checker)."""
+    for (W, T, H) in [(8, 3, 4096), (4, 129, 5120), (3, 5, 13)]:
+        xs, res, w = _inputs(dev, W, T, H)
+        g = 4096
+        bufs = [torch.full((T * H + 2 * g,), 0, dtype=torch.int16, device=dev) for _ in range(3)]
+        for b in bufs:
+            b.fill_(SENTINEL)
+        outs = [b[g:g + T * H].view(torch.bfloat16).view(T, H) for b in bufs]
+        farn.forward(xs, res, w, 1e-6, out=outs)
+        torch.cuda.synchronize()
+        for b in bufs:
+            h = b.cpu().numpy().view(np.uint16)
+            assert np.all(h[:g] == SENTINEL) and np.all(h[g + T * H:] == SENTINEL)
+        assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, 1e-6), "guards")
+
+
+def test_side_stream(O, dev):
+    p = synth.workload("decode")[4]
+    xs, res, w = synth.device_inputs(p, dev)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = farn.forward(xs, res, w, p.eps)
+    s.synchronize()
+    assert_parity([u16(t) for t in out], oracle_rows(O, xs, res, w, p.eps), "side stream")
+
+
+# ------------------------------------------------------ errors on the GPU
+def _sentinel_outputs(dev, T, H):
+    outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    for o in outs:
+        o.view(torch.int16).fill_(SENTINEL)
+    return outs
+
+
+def test_alias_error_writes_nothing(dev):
+    W, T, H = 4, 8, 2048
+    xs, res, w = _inputs(dev, W, T, H)
+    outs = _sentinel_outputs(dev, T, H)
+    with pytest.raises(farn.FarnError) as e:
+        farn.forward(xs, res, w, 1e-6, out=(outs[0], outs[0], outs[2]))
+    assert e.value.status == farn.FARN_ERR_ALIAS
+    with pytest.raises(farn.FarnError) as e:
+        farn.forward(xs, res, w, 1e-6, out=(xs[1], outs[1], outs[2]))
+    assert e.value.status == farn.FARN_ERR_ALIAS
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.all(u16(o) == SENTINEL)
+
+
+def test_bad_eps_and_shapes_raise(dev):
+    W, T, H = 2, 4, 64
+    xs, res, w = _inputs(dev, W, T, H)
+    with pytest.raises(farn.FarnError):
+        farn.forward(xs, res, w, float("nan"))
+    with pytest.raises(farn.FarnError):
+        farn.forward(xs, res, w, -1.0)
+    with pytest.raises(ValueError):
+        farn.forward(xs, res[:, :32].contiguous(), w, 1e-6)
+    with pytest.raises(TypeError):
+        farn.forward([x.float() for x in xs], res, w, 1e-6)
+
+
+def test_injected_launch_fault_launches_nothing(dev):
+    W, T, H = 4, 8, 2048
+    xs, res, w = _inputs(dev, W, T, H)
+    outs = _sentinel_outputs(dev, T, H)
+    os.environ["FARN_FAULT_INJECT"] = "launch"
+    try:
+        with pytest.raises(farn.FarnError) as e:
+            farn.forward(xs, res, w, 1e-6, out=outs)
+        assert e.value.status == farn.FARN_ERR_CUDA
+    finally:
+        os.environ.pop("FARN_FAULT_INJECT")
+    torch.cuda.synchronize()
+    for o in outs:
+        assert np.all(u16(o) == SENTINEL)
+    # the context stays usable afterwards
+    farn.forward(xs, res, w, 1e-6, out=outs)
+    torch.cuda.synchronize()
+    assert not np.all(u16(outs[2]) == SENTINEL)
+
+
+def test_injected_create_fault(dev):
+    os.environ["FARN_FAULT_INJECT"] = "create"
+    try:
+        with pytest.raises(farn.FarnError) as e:
+            farn.Context(0)
+        assert e.value.status == farn.FARN_ERR_CUDA
+    finally:
+        os.environ.pop("FARN_FAULT_INJECT")
