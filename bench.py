@@ -66,6 +66,8 @@ def parse_args(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="--impl reference: oracle time budget for the whole run")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override T of every call (small cases for profiling)")
     return ap.parse_args(argv)
 
 
@@ -316,6 +318,8 @@ def run_gpu(args):
 
     peak, peak_src = hbm_peak()
     problems = synth.workload(args.workload)
+    if args.rows is not None:
+        problems = [p.with_T(args.rows) for p in problems]
     step_bytes = sum(p.algorithmic_bytes() for p in problems)
     step_rows = sum(p.T for p in problems)
     set_bytes = step_bytes  # algorithmic bytes touched by one pass over one set
@@ -323,7 +327,10 @@ def run_gpu(args):
     n_sets = max(2, math.ceil(2 * l2 / set_bytes))
     n_sets = min(n_sets, max(1, int(40e9 // set_bytes)))
     ctx = farn.Context(local)
+    # One stream for everything: torch's graph replay, the calls and every
+    # CUDA event all use torch's current stream, so make it this one.
     stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
 
     # ---- inputs: n_sets rotating copies, generated on the device
     sets = []
@@ -351,67 +358,52 @@ def run_gpu(args):
         step(i % n_sets)
     stream.synchronize()
 
-    # ---- CUDA graphs: one per rotating set, with an event pair around
-    # every call so the per-kernel time comes from the timed region itself
+    # ---- CUDA graph: one replay is one rotation, i.e. one step over every
+    # input copy in turn (n_sets steps), so the host issues one replay per
+    # n_sets steps and never paces the GPU.
     use_graph = not args.no_graph
-    graphs, kev = [], []
-    ext_ok = True
+    graph = None
     if use_graph:
-        for k in range(n_sets):
-            g = torch.cuda.CUDAGraph()
-            evs = []
-            with torch.cuda.graph(g, stream=stream):
-                for call in sets[k]:
-                    e0 = e1 = None
-                    if ext_ok:
-                        try:
-                            e0 = torch.cuda.Event(enable_timing=True, external=True)
-                            e1 = torch.cuda.Event(enable_timing=True, external=True)
-                        except TypeError:
-                            ext_ok = False
-                    if e0 is not None:
-                        e0.record(stream)
-                    launch(call)
-                    if e1 is not None:
-                        e1.record(stream)
-                    evs.append((e0, e1))
-            graphs.append(g)
-            kev.append(evs)
-        for g in graphs:
-            g.replay()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for k in range(n_sets):
+                step(k)
+        graph.replay()
         stream.synchronize()
 
-    def run_step(i):
+    def run_steps(n):
+        """n steps (a multiple of n_sets when graphs are used)."""
         if use_graph:
-            graphs[i % n_sets].replay()
+            for _ in range(n // n_sets):
+                graph.replay()
         else:
-            step(i % n_sets)
+            for i in range(n):
+                step(i % n_sets)
 
     # ---- step count: about 1.5 s of GPU time unless given
     K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run_steps(4 * n_sets)
+    e1.record(stream)
+    e1.synchronize()
+    calib_ms = e0.elapsed_time(e1) / (4 * n_sets)
     if K is None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(20):
-            run_step(i)
-        e1.record(stream)
-        e1.synchronize()
-        per = e0.elapsed_time(e1) / 20 / 1e3
-        K = max(20, int(1.5 / max(per, 1e-7)))
-        K = (K + n_sets - 1) // n_sets * n_sets
+        K = max(20, int(1500.0 / max(calib_ms, 1e-4)))
+    if use_graph:
+        K = max(n_sets, (K + n_sets - 1) // n_sets * n_sets)
 
     sampler = ClockSampler(gpu_id_for(local)).start() if rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
-    for i in range(args.warmup):
-        run_step(i)
+    time.sleep(0.5 if sampler else 0)
+    run_steps(max(args.warmup, 1) if not use_graph else
+              max(n_sets, (args.warmup + n_sets - 1) // n_sets * n_sets))
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     ev0.record(stream)
-    for i in range(K):
-        run_step(i)
+    run_steps(K)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
@@ -422,7 +414,12 @@ def run_gpu(args):
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
-    time.sleep(0.2 if sampler else 0)
+
+    # ---- per-call kernel time, right after the timed steps and under the
+    # same clock sampling: each call alone, back to back over the input
+    # copies in one CUDA graph, CUDA events on the launching stream.
+    per_call = time_calls_alone(sets, problems, stream, ctx)
+    time.sleep(0.3 if sampler else 0)
     if sampler:
         sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
@@ -431,38 +428,22 @@ def run_gpu(args):
     value = world * step_bytes * K / secs / 1e9
     rows_per_s = world * step_rows * K / secs
 
-    # ---- per-call kernel times (last replay of every graph = the last
-    # n_sets steps of the timed region)
-    per_call = []
-    for j, p in enumerate(problems):
-        durs = []
-        if use_graph and ext_ok:
-            for k in range(n_sets):
-                e0, e1 = kev[k][j]
-                durs.append(e0.elapsed_time(e1))
-        per_call.append(dict(call=p.name, T=p.T, W=p.W, H=p.H,
-                             bytes=p.algorithmic_bytes(),
-                             kernel_us=(statistics.mean(durs) * 1e3) if durs else None))
-    if not (use_graph and ext_ok):
-        per_call = time_calls_alone(sets, problems, stream, per_call)
-    for c in per_call:
-        c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9 if c["kernel_us"] else None
-        c["frac"] = c["gbs"] / peak if c["gbs"] else None
-        v, cs, thr = farn.farn_plan(ctx.handle, *plan_args(sets[0][per_call.index(c)]))
+    for j, c in enumerate(per_call):
+        c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
+        c["frac"] = c["gbs"] / peak
+        v, cs, thr = farn.farn_plan(ctx.handle, *plan_args(sets[0][j]))
         c["variant"] = f"{v} cluster={cs} threads={thr}"
-    dom = max(per_call, key=lambda c: (c["kernel_us"] or 0.0))
-    dom_kernel_name = kernel_name(dom["variant"], dom["W"], dom["H"])
+    dom = max(per_call, key=lambda c: c["kernel_us"] * c["count_per_step"])
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": None,
-                "kernel": dom_kernel_name, "call": dom["call"],
+                "kernel": kernel_name(dom["variant"]), "call": dom["call"],
                 "algorithmic_bytes_per_launch": dom["bytes"],
                 "launch_us": dom["kernel_us"],
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs: copy bandwidth)"
+                "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)"
                 if peak_src == "measured" else "fallback 6.8 TB/s",
-                "timing": "CUDA events recorded inside the timed graphs around each call; "
-                          f"mean of the last {n_sets} replays"
-                if (use_graph and ext_ok) else "CUDA events around a graph of back-to-back "
-                                               "launches of the call alone"}
+                "timing": "CUDA events around a graph of back-to-back launches of this "
+                          "call alone over the rotating input copies, right after the "
+                          "timed steps"}
 
     # ---- end to end: pinned host inputs in, outputs back, every step
     e2e = None
@@ -484,7 +465,9 @@ def run_gpu(args):
                        "l2": f"inputs rotated over {n_sets} device copies "
                              f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB); "
                              "no flush",
-                       "launch": "CUDA graph replay per step" if use_graph else "direct launches",
+                       "launch": (f"CUDA graph, one replay per {n_sets} steps"
+                                  if use_graph else "direct launches"),
+                       "calibration_ms_per_step": calib_ms,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "rows_per_s": rows_per_s,
             "pct_hbm_peak": 100.0 * value / world / peak,
@@ -502,7 +485,7 @@ def run_gpu(args):
     return 0
 
 
-def kernel_name(variant, W, H):
+def kernel_name(variant):
     return "farn_vec_kernel" if not variant.startswith("generic") else "farn_generic_kernel"
 
 
@@ -512,27 +495,32 @@ def plan_args(call):
             outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr())
 
 
-def time_calls_alone(sets, problems, stream, per_call):
-    """Fallback when graph-captured events are unavailable: each call alone,
-    replayed back to back over the rotating sets in one CUDA graph."""
+def time_calls_alone(sets, problems, stream, ctx, min_reps=64):
+    """Mean launch duration of each call of a step, timed alone."""
     import torch
     import rank_sum_residual_gb300 as farn
+    out = []
+    n_sets = len(sets)
     for j, p in enumerate(problems):
+        reps = max(1, math.ceil(min_reps / n_sets)) * n_sets
         g = torch.cuda.CUDAGraph()
-        reps = max(1, 64 // len(sets)) * len(sets)
         with torch.cuda.graph(g, stream=stream):
             for i in range(reps):
-                q, xs, res, w, outs = sets[i % len(sets)][j]
-                farn.forward(xs, res, w, q.eps, out=outs, stream=stream)
+                q, xs, res, w, outs = sets[i % n_sets][j]
+                farn.forward(xs, res, w, q.eps, out=outs, ctx=ctx, stream=stream)
         g.replay()
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        g.replay()
+        for _ in range(3):
+            g.replay()
         e1.record(stream)
         e1.synchronize()
-        per_call[j]["kernel_us"] = e0.elapsed_time(e1) / reps * 1e3
-    return per_call
+        out.append(dict(call=p.name, T=p.T, W=p.W, H=p.H, bytes=p.algorithmic_bytes(),
+                        count_per_step=1, launches_timed=3 * reps,
+                        kernel_us=e0.elapsed_time(e1) / (3 * reps) * 1e3))
+        del g
+    return out
 
 
 def run_e2e(calls, problems, stream, dev, K, world, step_bytes):

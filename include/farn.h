@@ -82,7 +82,9 @@ int farn_create(farn_ctx **out, int device);
  *   residual     bf16 [T,H]
  *   weight       bf16 [H]
  *   eps          finite, >= 0 (fp32; added to the mean square inside sqrt)
- *   T            rows (tokens), >= 0; T == 0 returns FARN_OK, launches nothing
+ *   T            rows (tokens), >= 0; T == 0 returns FARN_OK and launches
+ *                nothing (the tensor pointers may then be NULL, as the data
+ *                pointers of empty tensors are)
  *   H            hidden size (row length), >= 1
  *   reduced_out, residual_out, norm_out   bf16 [T,H] outputs
  *   stream       CUDA stream (0 = legacy default stream)

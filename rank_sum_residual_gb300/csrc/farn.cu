@@ -29,6 +29,7 @@ struct farn_ctx {
   int force_variant;   // kVariantAuto unless FARN_VARIANT says otherwise
   int force_cluster;   // 0 = choose; else CTAs per row for the cluster variant
   int force_vpt;       // 0 = choose; else 16-byte vectors per thread
+  int pdl;             // launch with programmatic stream serialisation
 };
 
 namespace {
@@ -177,11 +178,14 @@ int farn_check_args(const void* const* partials, int W, const void* residual,
                     const void* norm_out) {
   if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1) return FARN_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 2 || (T > 0 && T > INT64_MAX / (2 * H))) return FARN_ERR_INVALID_ARG;
+  // With no rows nothing is read or written: empty tensors may have null
+  // data pointers.
+  if (T == 0) return FARN_OK;
   if (!residual || !weight || !reduced_out || !residual_out || !norm_out)
     return FARN_ERR_INVALID_ARG;
   for (int r = 0; r < W; ++r)
     if (!partials[r]) return FARN_ERR_INVALID_ARG;
-  if (H > INT64_MAX / 2 || (T > 0 && T > INT64_MAX / (2 * H))) return FARN_ERR_INVALID_ARG;
   const int64_t nb = T * H * 2, wb = H * 2;
   const void* outs[3] = {reduced_out, residual_out, norm_out};
   for (int i = 0; i < 3; ++i) {
@@ -253,6 +257,7 @@ int farn_create(farn_ctx** out, int device) {
   if (c->force_cluster != 0 && c->force_cluster != 1 && c->force_cluster != 2 &&
       c->force_cluster != 4 && c->force_cluster != 8 && c->force_cluster != 16)
     c->force_cluster = 0;
+  c->pdl = env_int("FARN_PDL", 1) != 0;
   c->force_vpt = env_int("FARN_VPT", 0);
   if (c->force_vpt != 0 && c->force_vpt != 1 && c->force_vpt != 2 && c->force_vpt != 4)
     c->force_vpt = 0;
@@ -335,13 +340,26 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)pl.cs;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = pl.cs > 1 ? 1 : 0;
+  // Attributes: the cluster shape of the split-row variant, and
+  // programmatic stream serialisation (the kernel waits for the previous
+  // grid with griddepcontrol.wait before touching global memory, so this
+  // only overlaps launch latency with the previous kernel's tail).
+  cudaLaunchAttribute attrs[2];
+  unsigned nattr = 0;
+  if (pl.cs > 1) {
+    attrs[nattr].id = cudaLaunchAttributeClusterDimension;
+    attrs[nattr].val.clusterDim.x = (unsigned)pl.cs;
+    attrs[nattr].val.clusterDim.y = 1;
+    attrs[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+  if (ctx->pdl) {
+    attrs[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = nattr;
 
   cudaError_t err;
   if (pl.variant == kVariantGeneric) {

@@ -125,6 +125,19 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   return v;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// When launched with programmatic stream serialisation the grid may start
+// while the previous kernel on the stream is still finishing.  pdl_wait()
+// blocks until that kernel has completed and its memory is visible, so no
+// global load or store may come before it.  pdl_trigger() lets the next
+// kernel start launching.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -157,6 +170,20 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   __shared__ float cta_ss;
 
   const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
+  // Small slices (decode-sized calls) are latency bound: their weight is
+  // fetched up front, alongside the partials.  Larger ones fetch it after
+  // the rank loop, where it holds no registers during the loads.
+  constexpr bool kEarlyWeight = VPT <= 2;
+  uint4 wv[VPT];
+
+  pdl_wait();
+  if (kEarlyWeight) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) wv[k] = ld_keep(wv4 + j);
+    }
+  }
 
   const int64_t rows_per_pass = gridDim.x / CS;
   int it = 0;
@@ -223,14 +250,17 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       }
     }
 
-    // The weight slice (cached: every row reads it) is fetched here so its
-    // latency hides behind the reduction below and it holds no registers
-    // during the rank loop.
-    uint4 wv[VPT];
+    // Last loads of this row issued: the next kernel may start launching.
+    if (row + rows_per_pass >= p.T) pdl_trigger();
+
+    // The weight slice (cached: every row reads it) is fetched here for
+    // large slices, so its latency hides behind the reduction below.
+    if (!kEarlyWeight) {
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int j = tid + k * blockDim.x;
-      if (j < sv) wv[k] = ld_keep(wv4 + j);
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * blockDim.x;
+        if (j < sv) wv[k] = ld_keep(wv4 + j);
+      }
     }
 
     // a3: CTA sum of squares (warp butterfly, then the warps' sums in
@@ -298,6 +328,7 @@ farn_generic_kernel(const __grid_constant__ Params p) {
   uint16_t* red_out = reinterpret_cast<uint16_t*>(p.reduced);
   uint16_t* ro_out = reinterpret_cast<uint16_t*>(p.residual_out);
   uint16_t* nrm_out = reinterpret_cast<uint16_t*>(p.norm_out);
+  pdl_wait();
   int it = 0;
   for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
     const int64_t off = row * p.H;

@@ -78,6 +78,11 @@ def test_invalid_arguments(kw):
     assert check(**kw) == farn.FARN_ERR_INVALID_ARG
 
 
+def test_zero_rows_accept_null_tensors():
+    # empty tensors have null data pointers; with T == 0 nothing is touched
+    assert farn.farn_check_args([0, 0], 2, 0, 0, 1e-6, 0, 64, 0, 0, 0) == 0
+
+
 def test_null_partials_array():
     assert farn.farn_check_args(None, 2, RES, WT, 1e-6, 4, 64, RED, RO, NRM) \
         == farn.FARN_ERR_INVALID_ARG

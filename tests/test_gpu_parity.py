@@ -144,15 +144,17 @@ def test_plan_choices(dev):
     c = farn.Context(0)
     try:
         def plan(W, T, H, off=0):
-            a = 0x10000000 + off
-            return farn.farn_plan(c.handle, W, T, H, [a] * W, a + 0x1000000,
-                                  a + 0x2000000, a + 0x3000000, a + 0x4000000, a + 0x5000000)
+            # fake, never-dereferenced addresses 4 GiB apart
+            a = (1 << 40) + off
+            g = 1 << 32
+            return farn.farn_plan(c.handle, W, T, H, [a] * W, a + g, a + 2 * g,
+                                  a + 3 * g, a + 4 * g, a + 5 * g)
         assert plan(8, 8192, 8192)[0] == "row"
         assert plan(8, 1, 4096)[0] == "cluster"
         assert plan(8, 1, 4096)[1] >= 8
         assert plan(4, 16, 13)[0] == "generic"          # H % 8 != 0
         assert plan(4, 16, 2048, off=2)[0] == "generic"  # misaligned
-        assert plan(4, 16, 32768)[0] == "generic"       # longer than one CTA
+        assert plan(4, 4096, 32768)[0] == "generic"     # longer than one CTA
     finally:
         c.close()
 
@@ -219,8 +221,7 @@ def test_special_values(O, dev):
     big = torch.tensor(3.0e38, dtype=torch.bfloat16)
     for x in xs:
         x[2, 5] = big
-    tiny = torch.tensor([1]).to(torch.int16).view(torch.bfloat16)   # 2^-133
-    for x in xs:
+    for x in xs:                                      # 2^-133 everywhere
         x[3].view(torch.int16)[:] = 1
     res[3].zero_()
     out = farn.forward(xs, res, w, 1e-6)
@@ -228,11 +229,11 @@ def test_special_values(O, dev):
     got = [u16(t) for t in out]
     want = oracle_rows(O, xs, res, w, 1e-6)
     assert_parity(got, want, "special values")
-    assert np.all(got[0][0] == 0) and np.all(got[2][0] == 0)
+    # a zero row stays zero (-0 where the weight is negative)
+    assert np.all(got[0][0] == 0) and np.all((got[2][0] & 0x7FFF) == 0)
     assert np.isnan(out[2][1].float().cpu().numpy()).all()
     assert got[0][2, 5] == 0x7F80                     # +inf
     assert np.all(got[0][3] == 4)                     # 4 * 2^-133, kept, not flushed
-    del tiny
 
 
 def test_in_place_residual(O, dev):
@@ -339,3 +340,37 @@ def test_injected_create_fault(dev):
         assert e.value.status == farn.FARN_ERR_CUDA
     finally:
         os.environ.pop("FARN_FAULT_INJECT")
+
+
+# ------------------------------------------- back-to-back dependent calls
+@pytest.mark.parametrize("pdl", [1, 0])
+def test_dependent_chain(O, dev, pdl):
+    """Each call reads what the previous call wrote (its reduced becomes the
+    next rank-0 partial, its residual_out the next residual) and overwrites
+    buffers that the previous call read, with programmatic dependent launch
+    on and off: the kernel must wait for its predecessor before any global
+    access.  reduced and residual_out are exact, so the whole chain must
+    match the oracle's chain bit for bit."""
+    W, T, H, n = 4, 3, 4096, 12
+    xs, res, w = _inputs(dev, W, T, H, seed=23)
+    hx = [u16(x) for x in xs]
+    hres, hw = u16(res), u16(w)
+    ctx = make_ctx(FARN_PDL=pdl)
+    try:
+        bufs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(6)]
+        cur_x, cur_res = list(xs), res
+        for i in range(n):
+            red, ro, nrm = bufs[0:3] if i % 2 == 0 else bufs[3:6]
+            farn.forward(cur_x, cur_res, w, 1e-6, out=(red, ro, nrm), ctx=ctx)
+            cur_x = [red] + cur_x[1:]
+            cur_res = ro
+        torch.cuda.synchronize()
+        got = [u16(red), u16(ro), u16(nrm)]
+    finally:
+        ctx.close()
+    ox, ores = hx, hres
+    for i in range(n):
+        want = O.forward(ox, ores, hw, 1e-6)
+        ox = [want[0]] + ox[1:]
+        ores = want[1]
+    assert_parity(got, want, f"chain of {n} dependent calls, pdl={pdl}")
