@@ -418,7 +418,7 @@ def run_gpu(args):
     # ---- per-call kernel time, right after the timed steps and under the
     # same clock sampling: each call alone, back to back over the input
     # copies in one CUDA graph, CUDA events on the launching stream.
-    per_call = time_calls_alone(sets, problems, stream, ctx)
+    per_call = time_calls_alone(problems, dev, ctx, l2)
     time.sleep(0.3 if sampler else 0)
     if sampler:
         sampler.stop()
@@ -442,8 +442,8 @@ def run_gpu(args):
                 "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)"
                 if peak_src == "measured" else "fallback 6.8 TB/s",
                 "timing": "CUDA events around a graph of back-to-back launches of this "
-                          "call alone over the rotating input copies, right after the "
-                          "timed steps"}
+                          "call alone over its own rotating copies (> 2 x L2), right "
+                          "after the timed steps"}
 
     # ---- end to end: pinned host inputs in, outputs back, every step
     e2e = None
@@ -495,31 +495,47 @@ def plan_args(call):
             outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr())
 
 
-def time_calls_alone(sets, problems, stream, ctx, min_reps=64):
-    """Mean launch duration of each call of a step, timed alone."""
+def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
+    """Mean launch duration of each call of a step, timed alone and from
+    HBM: each call gets its own rotation of input/output copies, together
+    at least twice the L2 size, laid out as one [copies, T, H] tensor per
+    operand and launched back to back from one CUDA graph."""
     import torch
     import rank_sum_residual_gb300 as farn
+    import synth
     out = []
-    n_sets = len(sets)
-    for j, p in enumerate(problems):
-        reps = max(1, math.ceil(min_reps / n_sets)) * n_sets
+    for p in problems:
+        copies = max(2, math.ceil(2 * l2_bytes / p.algorithmic_bytes()))
+        xs = [torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
+              for _ in range(p.W)]
+        res = torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
+        w = torch.empty((p.H,), dtype=torch.bfloat16, device=dev)
+        for r, x in enumerate(xs):
+            synth.fill_device(x, p.seed + 1, r, p.x)
+        synth.fill_device(res, p.seed + 1, synth.STREAM_RESIDUAL, p.residual)
+        synth.fill_device(w, p.seed + 1, synth.STREAM_WEIGHT, p.weight)
+        outs = [torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
+                for _ in range(3)]
+        reps = max(min_launches, copies)
         g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
+        with torch.cuda.graph(g):
             for i in range(reps):
-                q, xs, res, w, outs = sets[i % n_sets][j]
-                farn.forward(xs, res, w, q.eps, out=outs, ctx=ctx, stream=stream)
+                c = i % copies
+                farn.forward([x[c] for x in xs], res[c], w, p.eps,
+                             out=tuple(o[c] for o in outs), ctx=ctx)
         g.replay()
-        stream.synchronize()
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record()
         for _ in range(3):
             g.replay()
-        e1.record(stream)
+        e1.record()
         e1.synchronize()
         out.append(dict(call=p.name, T=p.T, W=p.W, H=p.H, bytes=p.algorithmic_bytes(),
-                        count_per_step=1, launches_timed=3 * reps,
+                        count_per_step=1, launches_timed=3 * reps, rotating_copies=copies,
                         kernel_us=e0.elapsed_time(e1) / (3 * reps) * 1e3))
-        del g
+        del g, xs, res, w, outs
+        torch.cuda.empty_cache()
     return out
 
 

@@ -67,9 +67,10 @@ typedef struct farn_ctx farn_ctx;
 /* Create a context for CUDA device `device` (this is the one-time set-up
  * that the page's host side does at initialisation, Implementation
  * section 4, "host-side C ABI"; there is no communicator to bootstrap).
- * Queries the SM count and cluster limits and sets kernel attributes.
- * Enqueues no work and allocates no device memory.  The caller's current
- * device is left as it was.
+ * Queries the SM count and cluster limits, sets kernel attributes and
+ * allocates one 256-byte device block (the status word of the TMA-staged
+ * kernel, see farn_device_status).  The caller's current device is left
+ * as it was.
  * Returns FARN_ERR_INVALID_ARG if out is NULL or device < 0,
  * FARN_ERR_CUDA if the device cannot be queried, FARN_ERR_NOMEM. */
 int farn_create(farn_ctx **out, int device);
@@ -109,6 +110,15 @@ int farn_check_args(const void *const *partials, int W,
                     const void *reduced_out, const void *residual_out,
                     const void *norm_out);
 
+/* Read and clear the context's device status word (blocking: waits for
+ * the device).  0 means every wait of the TMA-staged kernel completed; a
+ * non-zero value has one bit per kind of wait that gave up after its time
+ * limit (2 s): 1 a consumer waiting for a staged row, 2 the producer
+ * waiting for a free stage, 4 a consumer in the row reduction, 8 the
+ * producer draining its copies.  The kernel that gave up left its outputs
+ * incomplete.  Returns FARN_ERR_INVALID_ARG or FARN_ERR_CUDA on failure. */
+int farn_device_status(const farn_ctx *ctx, int *status);
+
 /* Release a context (NULL is accepted).  Returns FARN_OK. */
 int farn_destroy(farn_ctx *ctx);
 
@@ -117,7 +127,8 @@ const char *farn_status_string(int status);
 
 /* Which kernel variant farn_forward would launch for this shape and these
  * pointers, without launching: 0 row (one CTA per row), 1 cluster (a
- * cluster of CTAs splits each row), 2 generic (any H or alignment).
+ * cluster of CTAs splits each row), 2 generic (any H or alignment), 3 bulk
+ * (persistent CTAs that stage rows in shared memory with TMA bulk copies).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */
 int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,

@@ -23,7 +23,7 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "FARN_MAX_W", "FarnError", "Context", "build_library", "library_path",
     "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
-    "farn_plan", "farn_status_string", "forward", "VARIANTS",
+    "farn_plan", "farn_status_string", "farn_device_status", "forward", "VARIANTS",
 ]
 
 FARN_MAX_W = 32
@@ -33,7 +33,7 @@ FARN_ERR_UNSUPPORTED = -2
 FARN_ERR_ALIAS = -3
 FARN_ERR_CUDA = -4
 FARN_ERR_NOMEM = -5
-VARIANTS = {0: "row", 1: "cluster", 2: "generic"}
+VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk"}
 
 _lib = None
 
@@ -67,6 +67,8 @@ def _load():
                                   cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                   ctypes.POINTER(i32)]
         lib.farn_plan.restype = i32
+        lib.farn_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        lib.farn_device_status.restype = i32
         lib.farn_status_string.argtypes = [i32]
         lib.farn_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -109,6 +111,15 @@ def farn_forward(ctx, partials, W, residual, weight, eps, T, H,
         int(T), int(H), ctypes.c_void_p(int(reduced_out)),
         ctypes.c_void_p(int(residual_out)), ctypes.c_void_p(int(norm_out)),
         ctypes.c_void_p(int(stream)))
+
+
+def farn_device_status(ctx: int) -> int:
+    """C ``farn_device_status``: read and clear the device status word."""
+    v = ctypes.c_int()
+    st = _load().farn_device_status(ctypes.c_void_p(ctx), ctypes.byref(v))
+    if st != FARN_OK:
+        raise FarnError(st, "farn_device_status")
+    return v.value
 
 
 def farn_check_args(partials, W, residual, weight, eps, T, H, reduced_out,

@@ -20,7 +20,13 @@
 
 static_assert(FARN_MAX_W == farn::kMaxW, "FARN_MAX_W and kernel limit differ");
 
-enum { kVariantRow = 0, kVariantCluster = 1, kVariantGeneric = 2, kVariantAuto = -1 };
+enum {
+  kVariantRow = 0,
+  kVariantCluster = 1,
+  kVariantGeneric = 2,
+  kVariantBulk = 3,
+  kVariantAuto = -1
+};
 
 struct farn_ctx {
   int device;
@@ -30,9 +36,25 @@ struct farn_ctx {
   int force_cluster;   // 0 = choose; else CTAs per row for the cluster variant
   int force_vpt;       // 0 = choose; else 16-byte vectors per thread
   int pdl;             // launch with programmatic stream serialisation
+  int64_t small_t;     // below this many rows a call counts as latency bound
+  int bulk;            // 1: the TMA-staged kernel serves long inputs by default
+  int bulk_ctas;       // resident bulk CTAs per SM (1 or 2)
+  int max_smem;        // opt-in shared memory per CTA, bytes
+  int* d_status;       // device status word of the bulk kernel (256 B block)
 };
 
 namespace {
+
+typedef void (*VecKernel)(const farn::Params);
+
+VecKernel pick_bulk(int vpt) {
+  switch (vpt) {
+    case 1: return &farn::farn_bulk_kernel<1>;
+    case 2: return &farn::farn_bulk_kernel<2>;
+    case 4: return &farn::farn_bulk_kernel<4>;
+  }
+  return nullptr;
+}
 
 struct Plan {
   int variant;
@@ -40,9 +62,40 @@ struct Plan {
   int vpt;      // vectors per thread
   int threads;  // threads per CTA
   int64_t grid;
+  uint32_t stages;        // bulk: ring stages
+  uint32_t stage_stride;  // bulk: bytes per stage
+  size_t smem;            // bulk: dynamic shared memory bytes
 };
 
-typedef void (*VecKernel)(const farn::Params);
+// Bulk plan: one producer warp + enough consumer warps for the row at up to
+// 4 vectors per thread; a ring of as many row-sized stages as fit.
+bool make_bulk_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
+  const int64_t hv = H / 8;
+  int vpt = hv > 256 ? 4 : (hv > 128 ? 2 : 1);
+  if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
+  const int64_t nct = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
+  const int bound = vpt >= 4 ? farn::BulkBounds<4>::kThreads
+                             : (vpt == 2 ? farn::BulkBounds<2>::kThreads
+                                         : farn::BulkBounds<1>::kThreads);
+  if (nct + 32 > bound || !pick_bulk(vpt)) return false;
+  const uint32_t stride = (uint32_t)((H * 2 + 127) / 128 * 128);
+  const size_t budget = (size_t)ctx->max_smem / (size_t)ctx->bulk_ctas;
+  const size_t fixed = sizeof(farn::BulkBarriers) + 128;
+  if (budget <= fixed) return false;
+  size_t ns = (budget - fixed) / stride;
+  if (ns > farn::kBulkMaxStages) ns = farn::kBulkMaxStages;
+  if (ns < 4) return false;
+  pl->variant = kVariantBulk;
+  pl->cs = 1;
+  pl->vpt = vpt;
+  pl->threads = (int)nct + 32;
+  const int64_t resident = (int64_t)ctx->num_sms * ctx->bulk_ctas;
+  pl->grid = T < resident ? T : resident;
+  pl->stages = (uint32_t)ns;
+  pl->stage_stride = stride;
+  pl->smem = ns * stride + sizeof(farn::BulkBarriers);
+  return true;
+}
 
 template <int VPT, int CS>
 VecKernel vec_kernel() { return &farn::farn_vec_kernel<VPT, CS>; }
@@ -99,29 +152,39 @@ int choose_vpt(int64_t sv) {
 int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   const int64_t hv = H / 8;
-  int want = ctx->force_variant;
+  const int want = ctx->force_variant;
+  const bool small = T < ctx->small_t;
+  pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
+  if (vec_ok && (want == kVariantBulk ||
+                 (want == kVariantAuto && ctx->bulk && !small && ctx->force_cluster == 0)) &&
+      make_bulk_plan(ctx, T, H, &pl)) {
+    *out = pl;
+    return FARN_OK;
+  }
+  if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   if (!vec_ok || want == kVariantGeneric) {
     pl.variant = kVariantGeneric;
     pl.cs = 1; pl.vpt = 1; pl.threads = 256;
     pl.grid = T;
   } else {
     int cs = 1;
-    if (want == kVariantCluster || want == kVariantAuto) {
-      if (ctx->force_cluster > 0) {
-        cs = ctx->force_cluster;
-      } else {
-        // Smallest power of two that puts about one CTA on every SM,
-        // while each CTA keeps at least one warp of 16-byte vectors.
-        const int cap = ctx->max_cluster;
-        while (T * cs < ctx->num_sms && cs * 2 <= cap && hv % (cs * 2) == 0 &&
-               hv / (cs * 2) >= 32)
-          cs *= 2;
-        if (want == kVariantCluster && cs == 1 && cap >= 2 && hv % 2 == 0) cs = 2;
-      }
-      if (cs > ctx->max_cluster || hv % cs != 0) return FARN_ERR_UNSUPPORTED;
+    if (ctx->force_cluster > 0 && want != kVariantRow) {
+      cs = ctx->force_cluster;
+    } else if (want != kVariantRow && small) {
+      // Few rows: the call is latency bound.  Split each row over a
+      // cluster so that every CTA owns about 64 16-byte vectors and each
+      // thread issues the loads of all ranks at once (one DRAM round trip
+      // per batch of 8 ranks) instead of looping over vectors.
+      const int cap = ctx->max_cluster;
+      while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64) cs *= 2;
     }
+    if (want == kVariantCluster && cs == 1 && ctx->max_cluster >= 2 && hv % 2 == 0) cs = 2;
+    if (cs > ctx->max_cluster || hv % cs != 0) return FARN_ERR_UNSUPPORTED;
     const int64_t sv = hv / cs;
-    int vpt = ctx->force_vpt > 0 ? ctx->force_vpt : choose_vpt(sv);
+    int vpt;
+    if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
+    else if (small && sv <= 512) vpt = 1;
+    else vpt = choose_vpt(sv);
     int64_t threads = (sv + vpt - 1) / vpt;
     threads = (threads + 31) / 32 * 32;
     if (threads > 512) {
@@ -252,12 +315,42 @@ int farn_create(farn_ctx** out, int device) {
     if (!strcmp(v, "row")) c->force_variant = kVariantRow;
     else if (!strcmp(v, "cluster")) c->force_variant = kVariantCluster;
     else if (!strcmp(v, "generic")) c->force_variant = kVariantGeneric;
+    else if (!strcmp(v, "bulk")) c->force_variant = kVariantBulk;
+  }
+  c->bulk = env_int("FARN_BULK", 0) != 0;
+  c->bulk_ctas = env_int("FARN_BULK_CTAS", 1) == 2 ? 2 : 1;
+  c->max_smem = 0;
+  c->d_status = nullptr;
+  if (cudaDeviceGetAttribute(&c->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+      cudaSuccess) {
+    delete c;
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  for (int vpt = 1; vpt <= 4; vpt *= 2) {
+    if (cudaFuncSetAttribute((const void*)pick_bulk(vpt),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem) !=
+        cudaSuccess) {
+      delete c;
+      cudaGetLastError();
+      return FARN_ERR_CUDA;
+    }
+  }
+  // The bulk kernel's status word: set on a bounded-wait timeout, read and
+  // cleared by farn_device_status.
+  if (cudaMalloc((void**)&c->d_status, 256) != cudaSuccess ||
+      cudaMemset(c->d_status, 0, 256) != cudaSuccess) {
+    if (c->d_status) cudaFree(c->d_status);
+    delete c;
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
   }
   c->force_cluster = env_int("FARN_CLUSTER", 0);
   if (c->force_cluster != 0 && c->force_cluster != 1 && c->force_cluster != 2 &&
       c->force_cluster != 4 && c->force_cluster != 8 && c->force_cluster != 16)
     c->force_cluster = 0;
   c->pdl = env_int("FARN_PDL", 1) != 0;
+  c->small_t = env_int("FARN_SMALL_T", c->num_sms);
   c->force_vpt = env_int("FARN_VPT", 0);
   if (c->force_vpt != 0 && c->force_vpt != 1 && c->force_vpt != 2 && c->force_vpt != 4)
     c->force_vpt = 0;
@@ -266,7 +359,28 @@ int farn_create(farn_ctx** out, int device) {
 }
 
 int farn_destroy(farn_ctx* ctx) {
-  delete ctx;
+  if (ctx) {
+    if (ctx->d_status) {
+      DeviceGuard g(ctx->device);
+      cudaFree(ctx->d_status);
+      cudaGetLastError();
+    }
+    delete ctx;
+  }
+  return FARN_OK;
+}
+
+int farn_device_status(const farn_ctx* ctx, int* status) {
+  if (!ctx || !status) return FARN_ERR_INVALID_ARG;
+  DeviceGuard g(ctx->device);
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  int v = 0;
+  if (cudaMemcpy(&v, ctx->d_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ctx->d_status, 0, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  *status = v;
   return FARN_OK;
 }
 
@@ -331,6 +445,9 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   prm.H = H;
   prm.W = W;
   prm.eps = eps;
+  prm.err = ctx->d_status;
+  prm.stages = pl.stages;
+  prm.stage_stride = pl.stage_stride;
 
   DeviceGuard g(ctx->device);
   if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
@@ -338,7 +455,7 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
   cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
   // Attributes: the cluster shape of the split-row variant, and
   // programmatic stream serialisation (the kernel waits for the previous
@@ -364,6 +481,8 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   cudaError_t err;
   if (pl.variant == kVariantGeneric) {
     err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel, prm);
+  } else if (pl.variant == kVariantBulk) {
+    err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm);
   } else {
     VecKernel k = pick_vec(pl.vpt, pl.cs);
     err = cudaLaunchKernelEx(&cfg, k, prm);

@@ -44,6 +44,10 @@ struct Params {
   int64_t H;     // elements per row
   int W;         // partials
   float eps;
+  // bulk (TMA-staged) kernel only
+  int* err;               // device status word, bits of kBulkErr* on a timeout
+  uint32_t stages;        // shared-memory ring stages
+  uint32_t stage_stride;  // bytes between stages (row bytes rounded to 128)
 };
 
 // ----------------------------------------------------------- bf16 helpers
@@ -109,20 +113,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Read a float from the shared memory of CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+// Write a float into the shared memory of CTA `rank` of this cluster, at
+// the address that `local` has in this CTA.
+__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
   uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
 }
 
 // ------------------------------------------- programmatic dependent launch
@@ -167,7 +167,7 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   const float Hf = (float)p.H;
 
   __shared__ float warp_ss[2][32];
-  __shared__ float cta_ss;
+  __shared__ float cluster_ss[2][CS];   // [row parity][CTA rank in cluster]
 
   const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
   // Small slices (decode-sized calls) are latency bound: their weight is
@@ -273,20 +273,20 @@ farn_vec_kernel(const __grid_constant__ Params p) {
     for (int w = 0; w < nwarps; ++w) tot += ws[w];
 
     if (CS > 1) {
-      // Cluster: the CTAs' totals through DSMEM, summed in CTA-rank order
-      // by every warp (lane c fetches CTA c's total).
-      if (tid == 0) cta_ss = tot;
+      // Cluster: thread c pushes this CTA's total into slot [slice] of CTA
+      // c through DSMEM; one cluster barrier (release/acquire) later every
+      // CTA holds all CS totals in its own shared memory and sums them in
+      // CTA-rank order, so all CTAs of the row get the same rstd.  No
+      // remote access follows the barrier, so a CTA may exit right after
+      // it; the row-parity double buffer keeps the next row's pushes off
+      // slots a slower peer is still reading.
+      float* slots = cluster_ss[it & 1];
+      if (tid < CS) st_dsmem_f32(&slots[slice], (uint32_t)tid, tot);
       cluster_arrive_release();
       cluster_wait_acquire();
-      float mine = 0.0f;
-      if (lane < CS) mine = ld_dsmem_f32(&cta_ss, (uint32_t)lane);
       tot = 0.0f;
 #pragma unroll
-      for (int c = 0; c < CS; ++c) tot += __shfl_sync(0xFFFFFFFFu, mine, c);
-      // Every thread has read what it needs from its peers; the matching
-      // wait below keeps each CTA's shared memory alive (and cta_ss
-      // unchanged) until all peers are done with it.
-      cluster_arrive_relaxed();
+      for (int c = 0; c < CS; ++c) tot += slots[c];
     }
 
     // a4: rstd with IEEE division and square root, then the normalised,
@@ -309,7 +309,6 @@ farn_vec_kernel(const __grid_constant__ Params p) {
                   make_uint4(n[0], n[1], n[2], n[3]));
       }
     }
-    if (CS > 1) cluster_wait_acquire();
   }
 }
 
@@ -357,6 +356,284 @@ farn_generic_kernel(const __grid_constant__ Params p) {
       const float q = __uint_as_float((uint32_t)ro_out[off + h] << 16);
       const float w = __uint_as_float((uint32_t)wt[h] << 16);
       nrm_out[off + h] = to_bf16((q * rstd) * w);
+    }
+  }
+}
+
+// ------------------------------------------- bulk (TMA-staged) kernel
+// Persistent and warp-specialised.  Warp 0 is the producer: one thread
+// streams, row after row, the row of every partial x[0..W-1] and then the
+// row of the residual (W+1 contiguous chunks of H*2 bytes) into a ring of
+// shared-memory stages with cp.async.bulk (the TMA engine's bulk copy),
+// each completing on the stage's "full" mbarrier.  The other warps are the
+// consumers: they read their 16-byte vectors of each stage in rank order,
+// release the stage on its "empty" mbarrier, and run the same per-element
+// arithmetic and epilogue as farn_vec_kernel.  The ring keeps up to
+// stages * H * 2 bytes in flight per SM without holding registers.
+//
+// Every wait is bounded: after kWaitLimitNs of globaltimer time the
+// waiting thread sets the CTA's abort flag and a bit in *p.err and
+// returns; the other threads see the flag in their own waits and leave;
+// the producer then waits (bounded again) for the copies it has in flight
+// before it exits, so no copy lands in a finished CTA's shared memory.
+constexpr uint32_t kBulkMaxStages = 16;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr int kBulkErrFull = 1;     // consumer gave up waiting for a stage
+constexpr int kBulkErrEmpty = 2;    // producer gave up waiting for a free stage
+constexpr int kBulkErrReduce = 4;   // consumer gave up in the row reduction
+constexpr int kBulkErrDrain = 8;    // producer gave up draining its copies
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completion counted in transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// Bounded phase wait.  false: gave up (time limit, or the CTA aborted).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile int* abort_flag, int* err, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, code);
+      return false;
+    }
+  }
+}
+
+// Dynamic shared memory: [stages][stage_stride] ring, then the barriers.
+struct BulkBarriers {
+  uint64_t full[kBulkMaxStages];
+  uint64_t empty[kBulkMaxStages];
+  uint64_t reduce[2];          // per row parity: one arrival per consumer warp
+  float warp_ss[2][32];
+  int abort_flag;
+};
+
+// Threads per CTA the bulk kernel is compiled for: one producer warp plus
+// up to 256 consumer threads at 4 vectors each, 512 at 2, 992 at 1.
+template <int VPT>
+struct BulkBounds {
+  static constexpr int kThreads = VPT >= 4 ? 288 : (VPT == 2 ? 544 : 1024);
+};
+
+template <int VPT>
+__global__ void __launch_bounds__(BulkBounds<VPT>::kThreads)
+farn_bulk_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const uint32_t NS = p.stages;
+  BulkBarriers* bb = reinterpret_cast<BulkBarriers*>(smem + (size_t)NS * p.stage_stride);
+  const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(&bb->full[0]);
+  const uint32_t empty0 = (uint32_t)__cvta_generic_to_shared(&bb->empty[0]);
+  const uint32_t reduce0 = (uint32_t)__cvta_generic_to_shared(&bb->reduce[0]);
+  volatile int* abort_flag = &bb->abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int ncw = (int)(blockDim.x >> 5) - 1;          // consumer warps
+  const int nct = ncw * 32;                            // consumer threads
+  const int64_t hv = p.H >> 3;
+  const uint32_t row_bytes = (uint32_t)(p.H * 2);
+  const int W = p.W;
+  const float Hf = (float)p.H;
+
+  if (tid == 0) {
+    for (uint32_t s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, (uint32_t)ncw);
+    }
+    mbar_init(reduce0, (uint32_t)ncw);
+    mbar_init(reduce0 + 8, (uint32_t)ncw);
+    bb->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    uint64_t q = 0;                       // chunks issued so far
+    bool ok = true;
+    for (int64_t row = blockIdx.x; row < p.T && ok; row += gridDim.x) {
+      const int64_t off = row * (int64_t)row_bytes;
+      for (int c = 0; c <= W; ++c, ++q) {
+        const uint32_t s = (uint32_t)(q % NS);
+        const uint64_t n = q / NS;
+        if (n > 0 && !wait_phase(empty0 + 8 * s, (uint32_t)((n - 1) & 1), abort_flag, p.err,
+                                 kBulkErrEmpty)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* src =
+            reinterpret_cast<const unsigned char*>(c < W ? p.x[c] : p.residual) + off;
+        mbar_arrive_expect_tx(full0 + 8 * s, row_bytes);
+        bulk_g2s(ring + s * p.stage_stride, src, row_bytes, full0 + 8 * s);
+      }
+      if (row + gridDim.x >= p.T) pdl_trigger();
+    }
+    if (!ok) {
+      // Drain: the last min(q, NS) chunks may still be in flight.
+      const uint64_t first = q > NS ? q - NS : 0;
+      for (uint64_t k = first; k < q; ++k) {
+        const uint32_t s = (uint32_t)(k % NS);
+        const uint32_t par = (uint32_t)((k / NS) & 1);
+        if (mbar_try_wait(full0 + 8 * s, par)) continue;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(full0 + 8 * s, par)) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(p.err, kBulkErrDrain);
+            break;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int ctid = tid - 32;
+  const int cw = warp - 1;
+  uint4 wv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = ctid + k * nct;
+    if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+  }
+
+  uint64_t q = 0;
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+    const int64_t base = row * hv;
+    float acc[VPT][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
+    uint4 rv[VPT];
+
+    // a1: rank sum from the staged rows, rank order; then the residual.
+    for (int c = 0; c <= W; ++c, ++q) {
+      const uint32_t s = (uint32_t)(q % NS);
+      if (!wait_phase(full0 + 8 * s, (uint32_t)((q / NS) & 1), abort_flag, p.err,
+                      kBulkErrFull))
+        return;
+      const uint32_t stage = ring + s * p.stage_stride;
+      uint4 v[VPT];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = ctid + k * nct;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < hv) v[k] = ld_shared_v4(stage + 16u * (uint32_t)j);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (c < W) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) add8(acc[k], v[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) rv[k] = v[k];
+      }
+    }
+    if (row + gridDim.x >= p.T) pdl_trigger();
+
+    // a2 + a5 and the thread's part of a3.
+    uint4 ro[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = ctid + k * nct;
+      if (j < hv) {
+        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        uint32_t red[4], out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
+          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+          out[e] = pack_bf16x2(s0, s1);
+          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+          ss = fmaf(q0, q0, ss);
+          ss = fmaf(q1, q1, ss);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                  make_uint4(red[0], red[1], red[2], red[3]));
+        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+      }
+    }
+
+    // a3: consumer-warp sums through shared memory, one mbarrier per row
+    // parity (each consumer warp arrives once), summed in warp order.
+    ss = warp_sum(ss);
+    const int par = it & 1;
+    if (lane == 0) {
+      bb->warp_ss[par][cw] = ss;
+      mbar_arrive(reduce0 + 8 * par);
+    }
+    if (!wait_phase(reduce0 + 8 * par, (uint32_t)((it >> 1) & 1), abort_flag, p.err,
+                    kBulkErrReduce))
+      return;
+    float tot = 0.0f;
+    for (int w = 0; w < ncw; ++w) tot += bb->warp_ss[par][w];
+
+    // a4
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = ctid + k * nct;
+      if (j < hv) {
+        const uint32_t qv[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
+        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint32_t n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n0 = (bf_lo(qv[e]) * rstd) * bf_lo(w[e]);
+          const float n1 = (bf_hi(qv[e]) * rstd) * bf_hi(w[e]);
+          n[e] = pack_bf16x2(n0, n1);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                  make_uint4(n[0], n[1], n[2], n[3]));
+      }
     }
   }
 }

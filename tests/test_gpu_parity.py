@@ -120,7 +120,7 @@ def _variant_outputs(dev, p, ctx):
     dict(FARN_VARIANT="cluster", FARN_CLUSTER=2), dict(FARN_VARIANT="cluster", FARN_CLUSTER=4),
     dict(FARN_VARIANT="cluster", FARN_CLUSTER=8), dict(FARN_VARIANT="cluster", FARN_CLUSTER=16),
     dict(FARN_VARIANT="row", FARN_VPT=1), dict(FARN_VARIANT="row", FARN_VPT=2),
-    dict(FARN_VARIANT="row", FARN_VPT=4),
+    dict(FARN_VARIANT="row", FARN_VPT=4), dict(FARN_VARIANT="bulk"),
 ], ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
 @pytest.mark.parametrize("shape", [(8, 5, 4096), (4, 37, 5120), (16, 3, 7168)],
                          ids=lambda s: f"W{s[0]}T{s[1]}H{s[2]}")
@@ -136,8 +136,46 @@ def test_forced_variants_match_oracle_and_each_other(O, dev, env, shape):
         _, _, _, ref = _variant_outputs(dev, p, None)
         assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
         assert compare(got, ref)["norm_out"]["max_ulp"] <= 1
+        assert farn.farn_device_status(ctx.handle) == 0
     finally:
         ctx.close()
+
+
+@pytest.mark.parametrize("name,T", [("prefill", 1000), ("nonpow2", 613), ("wide", 300),
+                                    ("decode", 4096), ("c1", 777), ("small_h", 999)])
+def test_bulk_variant(O, dev, name, T):
+    """The TMA-staged persistent kernel on the five shapes' H, W and value
+    recipes; T larger than the resident grid, so CTAs loop over rows and
+    the shared-memory ring wraps many times."""
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        if name == "small_h":         # H = 1024: one vector per consumer thread
+            p = synth.Problem("small_h", 5, T, 1024, 1e-6, 9, synth.N01)
+        else:
+            p = synth.workload(name)[0].with_T(T)
+        xs, res, w = synth.device_inputs(p, dev)
+        outs = [torch.empty_like(res) for _ in range(3)]
+        plan = farn.farn_plan(ctx.handle, p.W, p.T, p.H, [x.data_ptr() for x in xs],
+                              res.data_ptr(), w.data_ptr(), *[o.data_ptr() for o in outs])
+        assert plan[0] == "bulk"
+        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx)
+        torch.cuda.synchronize()
+        assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, p.eps),
+                      f"bulk {name} T={T}")
+        assert farn.farn_device_status(ctx.handle) == 0
+    finally:
+        ctx.close()
+
+
+def test_bulk_full_size_sampled(O, dev):
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        p = synth.workload("prefill")[0]
+        run_and_check(O, p, dev, ctx=ctx, rows=sample_rows(p.T, 96, seed=5))
+        assert farn.farn_device_status(ctx.handle) == 0
+    finally:
+        ctx.close()
+        torch.cuda.empty_cache()
 
 
 def test_plan_choices(dev):
@@ -374,3 +412,16 @@ def test_dependent_chain(O, dev, pdl):
         ox = [want[0]] + ox[1:]
         ores = want[1]
     assert_parity(got, want, f"chain of {n} dependent calls, pdl={pdl}")
+
+
+def test_bulk_forced_on_unsupported_shape_is_an_error(dev):
+    """Forcing the TMA-staged kernel where its consumer warps cannot cover
+    the row (more than 256 consumer threads) is refused, not mis-run."""
+    ctx = make_ctx(FARN_VARIANT="bulk", FARN_VPT=2)
+    try:
+        xs, res, w = _inputs(dev, 4, 8, 5120)
+        with pytest.raises(farn.FarnError) as e:
+            farn.forward(xs, res, w, 1e-6, ctx=ctx)
+        assert e.value.status == farn.FARN_ERR_UNSUPPORTED
+    finally:
+        ctx.close()
