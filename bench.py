@@ -79,6 +79,18 @@ def dist_info():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); the
+    identity without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -409,11 +421,7 @@ def run_gpu(args):
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
 
     # ---- per-call kernel time, right after the timed steps and under the
     # same clock sampling: each call alone, back to back over the input
@@ -584,10 +592,7 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     return {"value": world * step_bytes * Ke / (ms / 1e3) / 1e9, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
             "ms_per_step": ms / Ke,
