@@ -143,6 +143,9 @@ int env_int(const char* name, int dflt) {
 // Vectors per thread for a slice of sv 16-byte vectors (the vector kernel
 // takes at most 512 threads, so slices of up to 2048 vectors, H <= 16384
 // for one CTA per row).
+// Below this many rows a latency-bound call splits rows over a cluster.
+constexpr int64_t kClusterRowsMax = 8;
+
 int choose_vpt(int64_t sv) {
   if (sv >= 512) return 4;
   if (sv >= 128) return 2;
@@ -170,12 +173,13 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out)
     int cs = 1;
     if (ctx->force_cluster > 0 && want != kVariantRow) {
       cs = ctx->force_cluster;
-    } else if (want != kVariantRow && small) {
-      // Few rows: the call is latency bound.  Split each row over a
-      // cluster so that every CTA owns about 64 16-byte vectors and each
-      // thread issues the loads of all ranks at once (one DRAM round trip
-      // per batch of 8 ranks) instead of looping over vectors.
-      const int cap = ctx->max_cluster;
+    } else if (want != kVariantRow && small && T < kClusterRowsMax) {
+      // A handful of rows: split each row over a cluster so that every
+      // CTA owns about 64 16-byte vectors, spreading the row's loads over
+      // up to 8 SMs.  (Measured on GB300: best below 8 rows; from 8 rows
+      // one CTA per row with every thread loading all ranks at once is as
+      // fast and needs no cluster barrier.)
+      const int cap = ctx->max_cluster < 8 ? ctx->max_cluster : 8;
       while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64) cs *= 2;
     }
     if (want == kVariantCluster && cs == 1 && ctx->max_cluster >= 2 && hv % 2 == 0) cs = 2;
@@ -183,7 +187,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out)
     const int64_t sv = hv / cs;
     int vpt;
     if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
-    else if (small && sv <= 512) vpt = 1;
+    else if (small) vpt = sv <= 512 ? 1 : (sv <= 1024 ? 2 : 4);   // loads in one batch
     else vpt = choose_vpt(sv);
     int64_t threads = (sv + vpt - 1) / vpt;
     threads = (threads + 31) / 32 * 32;

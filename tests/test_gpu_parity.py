@@ -189,7 +189,8 @@ def test_plan_choices(dev):
                                   a + 3 * g, a + 4 * g, a + 5 * g)
         assert plan(8, 8192, 8192)[0] == "row"
         assert plan(8, 1, 4096)[0] == "cluster"
-        assert plan(8, 1, 4096)[1] >= 8
+        assert plan(8, 1, 4096)[1] == 8
+        assert plan(8, 64, 4096) == ("row", 1, 512)     # decode: all ranks at once
         assert plan(4, 16, 13)[0] == "generic"          # H % 8 != 0
         assert plan(4, 16, 2048, off=2)[0] == "generic"  # misaligned
         assert plan(4, 4096, 32768)[0] == "generic"     # longer than one CTA
@@ -416,10 +417,11 @@ def test_dependent_chain(O, dev, pdl):
 
 def test_bulk_forced_on_unsupported_shape_is_an_error(dev):
     """Forcing the TMA-staged kernel where its consumer warps cannot cover
-    the row (more than 256 consumer threads) is refused, not mis-run."""
-    ctx = make_ctx(FARN_VARIANT="bulk", FARN_VPT=2)
+    the row (at 4 vectors per thread, more than 256 consumer threads) is
+    refused, not mis-run."""
+    ctx = make_ctx(FARN_VARIANT="bulk", FARN_VPT=4)
     try:
-        xs, res, w = _inputs(dev, 4, 8, 5120)
+        xs, res, w = _inputs(dev, 4, 8, 12288)
         with pytest.raises(farn.FarnError) as e:
             farn.forward(xs, res, w, 1e-6, ctx=ctx)
         assert e.value.status == farn.FARN_ERR_UNSUPPORTED
