@@ -137,6 +137,44 @@ int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,
               const void *residual_out, const void *norm_out,
               int *variant, int *cluster_size, int *threads);
 
+/* farn_forward_noalloc - the fused operator for callers that cannot
+ * allocate device memory.  (No counterpart in the paper: the page's host
+ * side allocates a symmetric workspace; this entry point exists for
+ * callers that must not call cudaMalloc, e.g. code running inside another
+ * framework's plugin or allocator interface, where every device allocation
+ * has to go through that framework.)
+ *
+ * Same arithmetic, arguments, layout and error checks as farn_forward, but
+ * without a context: `device` names the CUDA device that owns the tensors.
+ * It always runs the TMA-staged kernel and allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library call.  The kernel's only
+ * memory beyond the caller's tensors is a 4-byte status word kept in a
+ * fixed 256-byte array that this library places in every GPU's memory for
+ * the life of the process; a call needs that one word whatever T, H and W
+ * are.  Shapes the TMA-staged kernel does not take (tensors not 16-byte
+ * aligned, H % 8 != 0, rows longer than 16384 elements) return
+ * FARN_ERR_UNSUPPORTED.
+ *
+ * The first call on a device sets that device up (finds the array's device
+ * address, reads the device limits, sets the kernels' shared-memory
+ * attribute); make that first call before any stream capture.  Every call
+ * clears the status word on `stream` before launching; the word is shared
+ * by all calls on the device, so calls that overlap on the GPU (different
+ * streams, no ordering between them) race on it.
+ *
+ * status_out: optional host pointer.  When non-NULL the call waits for the
+ * kernel to finish and stores the status word there (0 = every wait
+ * completed; bits as in farn_device_status).  When NULL the call is
+ * asynchronous like farn_forward.
+ * Returns FARN_OK, FARN_ERR_INVALID_ARG (as farn_forward, or device out of
+ * range), FARN_ERR_ALIAS, FARN_ERR_UNSUPPORTED or FARN_ERR_CUDA. */
+int farn_forward_noalloc(int device,
+                         const void *const *partials, int W,
+                         const void *residual, const void *weight, float eps,
+                         int64_t T, int64_t H,
+                         void *reduced_out, void *residual_out, void *norm_out,
+                         cudaStream_t stream, int *status_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ from ._build import LIB_PATH, build_library
 __all__ = [
     "FARN_MAX_W", "FarnError", "Context", "build_library", "library_path",
     "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
-    "farn_plan", "farn_status_string", "farn_device_status", "forward", "VARIANTS",
+    "farn_plan", "farn_status_string", "farn_device_status", "farn_forward_noalloc",
+    "forward", "VARIANTS",
 ]
 
 FARN_MAX_W = 32
@@ -67,6 +68,9 @@ def _load():
                                   cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                   ctypes.POINTER(i32)]
         lib.farn_plan.restype = i32
+        lib.farn_forward_noalloc.argtypes = [i32, pvp, i32, cvp, cvp, f32, i64, i64,
+                                             vp, vp, vp, vp, ctypes.POINTER(i32)]
+        lib.farn_forward_noalloc.restype = i32
         lib.farn_device_status.argtypes = [vp, ctypes.POINTER(i32)]
         lib.farn_device_status.restype = i32
         lib.farn_status_string.argtypes = [i32]
@@ -111,6 +115,23 @@ def farn_forward(ctx, partials, W, residual, weight, eps, T, H,
         int(T), int(H), ctypes.c_void_p(int(reduced_out)),
         ctypes.c_void_p(int(residual_out)), ctypes.c_void_p(int(norm_out)),
         ctypes.c_void_p(int(stream)))
+
+
+def farn_forward_noalloc(device, partials, W, residual, weight, eps, T, H,
+                         reduced_out, residual_out, norm_out, stream=0,
+                         want_status=False):
+    """C ``farn_forward_noalloc`` on raw device addresses (ints), for callers
+    that cannot allocate device memory: no context, nothing allocated.
+    Returns (status, device status word or None); asking for the word makes
+    the call wait for the kernel."""
+    word = ctypes.c_int(-1)
+    st = _load().farn_forward_noalloc(
+        int(device), _ptr_array(partials), int(W), ctypes.c_void_p(int(residual)),
+        ctypes.c_void_p(int(weight)), float(eps), int(T), int(H),
+        ctypes.c_void_p(int(reduced_out)), ctypes.c_void_p(int(residual_out)),
+        ctypes.c_void_p(int(norm_out)), ctypes.c_void_p(int(stream)),
+        ctypes.byref(word) if want_status else None)
+    return st, (word.value if want_status else None)
 
 
 def farn_device_status(ctx: int) -> int:

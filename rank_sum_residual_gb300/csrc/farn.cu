@@ -13,6 +13,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "farn.h"
@@ -494,6 +495,153 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   if (err != cudaSuccess) {
     cudaGetLastError();
     return FARN_ERR_CUDA;
+  }
+  return FARN_OK;
+}
+
+// ------------------------------------------------------------------------
+// No-allocation entry point.
+//
+// For callers that must not allocate device memory themselves or through
+// this library: code that runs inside another framework's plugin or
+// allocator interface, where every device allocation has to go through
+// that framework, and code that may not call cudaMalloc at all.  It runs
+// the TMA-staged kernel (farn_bulk_kernel), whose only memory beyond the
+// caller's inputs and outputs is its 4-byte status word; here that word
+// lives in the file-scope array below instead of a context's cudaMalloc'd
+// block, so nothing is allocated, ever.
+//
+// The array is kNoAllocScratchBytes (256) bytes per GPU and every GPU that
+// loads this library holds it until the process exits.  A call uses its
+// first 4 bytes, whatever T, H and W are; the shapes this entry point takes
+// are those of the TMA-staged kernel (16-byte aligned tensors, H % 8 == 0,
+// rows of at most 16384 elements for W <= 32), others are refused with
+// FARN_ERR_UNSUPPORTED.
+//
+// The array is shared by every call on the device and keeps the last
+// call's contents; each call clears the status word on its stream before
+// launching.  Calls that overlap on the GPU (different streams, no
+// ordering between them) race on that word.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) int g_farn_noalloc_scratch[kNoAllocScratchBytes / sizeof(int)];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+  std::once_flag once;
+  int status = FARN_ERR_CUDA;   // result of the set-up
+  int* scratch = nullptr;       // device address of g_farn_noalloc_scratch
+  int num_sms = 0;
+  int max_smem = 0;
+};
+
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: the scratch array's device
+// address (the array's name in host code is only a host-side stand-in),
+// the device limits and the bulk kernels' shared-memory attribute.
+void noalloc_setup(int device, NoAllocDevice* d) {
+  DeviceGuard g(device);
+  if (!g.ok) { cudaGetLastError(); d->status = FARN_ERR_CUDA; return; }
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_farn_noalloc_scratch) != cudaSuccess || !ptr ||
+      cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, device) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&d->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    d->status = FARN_ERR_CUDA;
+    return;
+  }
+  for (int vpt = 1; vpt <= 4; vpt *= 2) {
+    if (cudaFuncSetAttribute((const void*)pick_bulk(vpt),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, d->max_smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      d->status = FARN_ERR_CUDA;
+      return;
+    }
+  }
+  d->scratch = static_cast<int*>(ptr);
+  d->status = FARN_OK;
+}
+
+}  // namespace
+
+int farn_forward_noalloc(int device, const void* const* partials, int W, const void* residual,
+                         const void* weight, float eps, int64_t T, int64_t H,
+                         void* reduced_out, void* residual_out, void* norm_out,
+                         cudaStream_t stream, int* status_out) {
+  if (device < 0 || device >= kNoAllocMaxDevices) return FARN_ERR_INVALID_ARG;
+  int st = farn_check_args(partials, W, residual, weight, eps, T, H, reduced_out,
+                           residual_out, norm_out);
+  if (st != FARN_OK) return st;
+  if (T == 0) {
+    if (status_out) *status_out = 0;
+    return FARN_OK;
+  }
+  NoAllocDevice* d = &g_noalloc_dev[device];
+  std::call_once(d->once, noalloc_setup, device, d);
+  if (d->status != FARN_OK) return d->status;
+  static_assert(sizeof(int) <= kNoAllocScratchBytes, "status word must fit the scratch array");
+
+  if (!vector_path_ok(W, partials, residual, weight, reduced_out, residual_out, norm_out, H))
+    return FARN_ERR_UNSUPPORTED;
+  // The plan of the TMA-staged kernel for this device: a context-shaped
+  // description of the device on the stack (no device memory behind it).
+  farn_ctx dc;
+  memset(&dc, 0, sizeof dc);
+  dc.device = device;
+  dc.num_sms = d->num_sms;
+  dc.max_smem = d->max_smem;
+  dc.bulk_ctas = 1;
+  dc.force_variant = kVariantBulk;
+  Plan pl;
+  if (!make_bulk_plan(&dc, T, H, &pl)) return FARN_ERR_UNSUPPORTED;
+
+  farn::Params prm;
+  memset(&prm, 0, sizeof prm);
+  for (int r = 0; r < W; ++r) prm.x[r] = partials[r];
+  prm.residual = residual;
+  prm.weight = weight;
+  prm.reduced = reduced_out;
+  prm.residual_out = residual_out;
+  prm.norm_out = norm_out;
+  prm.T = T;
+  prm.H = H;
+  prm.W = W;
+  prm.eps = eps;
+  prm.err = d->scratch;
+  prm.stages = pl.stages;
+  prm.stage_stride = pl.stage_stride;
+
+  DeviceGuard g(device);
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  if (cudaMemsetAsync(d->scratch, 0, sizeof(int), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  if (cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm) != cudaSuccess) {
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  if (status_out) {
+    int v = 0;
+    if (cudaMemcpyAsync(&v, d->scratch, sizeof v, cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+      cudaGetLastError();
+      return FARN_ERR_CUDA;
+    }
+    *status_out = v;
   }
   return FARN_OK;
 }
