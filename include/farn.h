@@ -128,7 +128,9 @@ const char *farn_status_string(int status);
 /* Which kernel variant farn_forward would launch for this shape and these
  * pointers, without launching: 0 row (one CTA per row), 1 cluster (a
  * cluster of CTAs splits each row), 2 generic (any H or alignment), 3 bulk
- * (persistent CTAs that stage rows in shared memory with TMA bulk copies).
+ * (persistent CTAs that stage rows in shared memory with TMA bulk copies),
+ * 4 stage (persistent CTAs whose threads stage their own vectors in shared
+ * memory with cp.async).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */
 int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,

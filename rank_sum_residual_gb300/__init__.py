@@ -34,7 +34,7 @@ FARN_ERR_UNSUPPORTED = -2
 FARN_ERR_ALIAS = -3
 FARN_ERR_CUDA = -4
 FARN_ERR_NOMEM = -5
-VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk"}
+VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk", 4: "stage"}
 
 _lib = None
 

@@ -26,6 +26,7 @@ enum {
   kVariantCluster = 1,
   kVariantGeneric = 2,
   kVariantBulk = 3,
+  kVariantStage = 4,
   kVariantAuto = -1
 };
 
@@ -40,6 +41,12 @@ struct farn_ctx {
   int64_t small_t;     // below this many rows a call counts as latency bound
   int bulk;            // 1: the TMA-staged kernel serves long inputs by default
   int bulk_ctas;       // resident bulk CTAs per SM (1 or 2)
+  int stage;           // 1: the cp.async-staged kernel serves long inputs
+  int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
+  int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
+  int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
+  int stage_regs4;     // registers per thread of the stage kernels, 4 / 2 vectors
+  int stage_regs2;
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
 };
@@ -47,6 +54,19 @@ struct farn_ctx {
 namespace {
 
 typedef void (*VecKernel)(const farn::Params);
+
+VecKernel pick_stage(int vpt, int r) {
+  if (vpt == 2) {
+    if (r == 8) return &farn::farn_stage_kernel<2, 8>;
+    if (r == 12) return &farn::farn_stage_kernel<2, 12>;
+    if (r == 16) return &farn::farn_stage_kernel<2, 16>;
+  } else if (vpt == 4) {
+    if (r == 8) return &farn::farn_stage_kernel<4, 8>;
+    if (r == 12) return &farn::farn_stage_kernel<4, 12>;
+    if (r == 16) return &farn::farn_stage_kernel<4, 16>;
+  }
+  return nullptr;
+}
 
 VecKernel pick_bulk(int vpt) {
   switch (vpt) {
@@ -63,6 +83,7 @@ struct Plan {
   int vpt;      // vectors per thread
   int threads;  // threads per CTA
   int64_t grid;
+  int stage_r;            // stage: chunks in flight per thread
   uint32_t stages;        // bulk: ring stages
   uint32_t stage_stride;  // bulk: bytes per stage
   size_t smem;            // bulk: dynamic shared memory bytes
@@ -153,6 +174,57 @@ int choose_vpt(int64_t sv) {
   return 1;
 }
 
+// Stage plan.  Measured on GB300 (prefill / nonpow2 / wide shapes, and
+// H = 2048 / 4096 at T = 1k-8k): what matters is both the bytes each SM
+// keeps in flight and having at least two CTAs (or one of 512 threads) per
+// SM, so that one row's reduction overlaps another row's loads.  So:
+//   1. 4, then 2 vectors per thread, with the fewest CTAs per SM (2..4)
+//      that give >= 320 threads per SM and fit registers and shared memory;
+//   2. else one CTA per SM, 2 then 4 vectors per thread;
+// each with the largest of 16 / 12 / 8 chunks in flight per thread that fits.
+bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T) {
+  if (ctx->force_vpt > 0 && ctx->force_vpt != vpt) return false;
+  if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
+  const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
+  if (nt > 512) return false;
+  const int regs = vpt >= 4 ? ctx->stage_regs4 : ctx->stage_regs2;
+  if ((int64_t)regs * nt * ctas > 65536) return false;
+  const size_t budget = (size_t)ctx->max_smem / (size_t)ctas - 1024;
+  int r = 0;
+  const int cand_r[3] = {16, 12, 8};
+  for (int i = 0; i < 3 && !r; ++i) {
+    if (ctx->stage_r > 0 && cand_r[i] != ctx->stage_r) continue;
+    if ((size_t)cand_r[i] * vpt * nt * 16 <= budget) r = cand_r[i];
+  }
+  if (!r || !pick_stage(vpt, r)) return false;
+  pl->variant = kVariantStage;
+  pl->cs = 1;
+  pl->vpt = vpt;
+  pl->threads = (int)nt;
+  const int64_t resident = (int64_t)ctx->num_sms * ctas;
+  pl->grid = T < resident ? T : resident;
+  pl->stage_r = r;
+  pl->smem = (size_t)r * vpt * nt * 16;
+  return true;
+}
+
+bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
+  const int64_t hv = H / 8;
+  const int vpts[2] = {4, 2};
+  if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
+    return stage_fit(ctx, hv, 4, ctx->stage_ctas, pl, T) ||
+           stage_fit(ctx, hv, 2, ctx->stage_ctas, pl, T);
+  for (int i = 0; i < 2; ++i) {
+    const int vpt = vpts[i];
+    const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
+    int ctas = (int)((320 + nt - 1) / nt);
+    if (ctas < 2) ctas = 2;
+    for (; ctas <= 4; ++ctas)
+      if (stage_fit(ctx, hv, vpt, ctas, pl, T)) return true;
+  }
+  return stage_fit(ctx, hv, 2, 1, pl, T) || stage_fit(ctx, hv, 4, 1, pl, T);
+}
+
 int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   const int64_t hv = H / 8;
@@ -166,6 +238,15 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out)
     return FARN_OK;
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
+  pl.stage_r = 0;
+  if (vec_ok && (want == kVariantStage ||
+                 (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
+                  ctx->force_cluster == 0)) &&
+      make_stage_plan(ctx, T, H, &pl)) {
+    *out = pl;
+    return FARN_OK;
+  }
+  if (want == kVariantStage) return FARN_ERR_UNSUPPORTED;
   if (!vec_ok || want == kVariantGeneric) {
     pl.variant = kVariantGeneric;
     pl.cs = 1; pl.vpt = 1; pl.threads = 256;
@@ -321,7 +402,13 @@ int farn_create(farn_ctx** out, int device) {
     else if (!strcmp(v, "cluster")) c->force_variant = kVariantCluster;
     else if (!strcmp(v, "generic")) c->force_variant = kVariantGeneric;
     else if (!strcmp(v, "bulk")) c->force_variant = kVariantBulk;
+    else if (!strcmp(v, "stage")) c->force_variant = kVariantStage;
   }
+  c->stage = env_int("FARN_STAGE", 1) != 0;
+  c->stage_r = env_int("FARN_STAGE_R", 0);
+  c->stage_ctas = env_int("FARN_STAGE_CTAS", 0);
+  if (c->stage_ctas < 1 || c->stage_ctas > 4) c->stage_ctas = 0;
+  c->stage_min_t = env_int("FARN_STAGE_MIN_T", 2048);
   c->bulk = env_int("FARN_BULK", 0) != 0;
   c->bulk_ctas = env_int("FARN_BULK_CTAS", 1) == 2 ? 2 : 1;
   c->max_smem = 0;
@@ -339,6 +426,23 @@ int farn_create(farn_ctx** out, int device) {
       delete c;
       cudaGetLastError();
       return FARN_ERR_CUDA;
+    }
+  }
+  c->stage_regs4 = c->stage_regs2 = 0;
+  for (int vpt = 2; vpt <= 4; vpt *= 2) {
+    for (int r = 8; r <= 16; r += 4) {
+      // dynamic + static shared memory may not exceed the opt-in limit
+      cudaFuncAttributes fa;
+      if (cudaFuncGetAttributes(&fa, (const void*)pick_stage(vpt, r)) != cudaSuccess ||
+          cudaFuncSetAttribute((const void*)pick_stage(vpt, r),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {
+        delete c;
+        cudaGetLastError();
+        return FARN_ERR_CUDA;
+      }
+      int& regs = vpt >= 4 ? c->stage_regs4 : c->stage_regs2;
+      if (fa.numRegs > regs) regs = fa.numRegs;
     }
   }
   // The bulk kernel's status word: set on a bounded-wait timeout, read and
@@ -488,6 +592,8 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
     err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel, prm);
   } else if (pl.variant == kVariantBulk) {
     err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm);
+  } else if (pl.variant == kVariantStage) {
+    err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r), prm);
   } else {
     VecKernel k = pick_vec(pl.vpt, pl.cs);
     err = cudaLaunchKernelEx(&cfg, k, prm);

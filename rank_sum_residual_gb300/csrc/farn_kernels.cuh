@@ -638,4 +638,162 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
   }
 }
 
+// ------------------------------------------ stage (cp.async-staged) kernel
+// Persistent; each thread stages its own 16-byte vectors.  The chunks of a
+// CTA's rows, in order -- for each of its rows the row of x[0], ...,
+// x[W-1], then of the residual -- flow through R private shared-memory
+// slots per thread: the thread issues cp.async copies for chunk q+R while
+// it adds chunk q, so R chunks of its vectors are in flight without
+// holding registers, and the prefetch runs on across row boundaries while
+// the CTA reduces a row.  A thread only ever reads the slots it filled
+// itself, so the only waits are cp.async.wait_group (its own copies) and
+// the row reduction's __syncthreads.
+//
+// Shared memory: R * VPT * blockDim.x * 16 bytes, thread-interleaved so a
+// warp's 16-byte accesses are contiguous.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
+template <int VPT, int R>
+__global__ void __launch_bounds__(512)
+farn_stage_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (nt + 31) >> 5;
+  const int64_t hv = p.H >> 3;
+  const int W = p.W;
+  const float Hf = (float)p.H;
+  __shared__ float warp_ss[2][32];
+  const uint32_t slots = (uint32_t)__cvta_generic_to_shared(smem);
+  // slot s, vector k of this thread
+  auto slot_addr = [&](int s, int k) -> uint32_t {
+    return slots + (uint32_t)(((s * VPT + k) * nt + tid) * 16);
+  };
+
+  pdl_wait();
+  uint4 wv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = tid + k * nt;
+    if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+  }
+
+  // Chunk cursor for issuing: (row, c); chunks run over this CTA's rows.
+  int64_t irow = blockIdx.x;
+  int ic = 0;
+  auto issue_next = [&](int s) {
+    if (irow < p.T) {
+      const uint4* src = reinterpret_cast<const uint4*>(ic < W ? p.x[ic] : p.residual) +
+                         irow * hv;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * nt;
+        if (j < hv) cp_async16(slot_addr(s, k), src + j);
+      }
+      if (++ic > W) { ic = 0; irow += gridDim.x; }
+    }
+    cp_async_commit();   // one group per chunk, empty past the last row
+  };
+#pragma unroll
+  for (int s = 0; s < R; ++s) issue_next(s);
+
+  int q = 0;     // chunk being consumed
+  int it = 0;
+  int res_slot = 0;
+  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+    const int64_t base = row * hv;
+    float acc[VPT][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
+    uint4 rv[VPT];
+    // a1 in rank order, then the residual chunk.
+    for (int c = 0; c <= W; ++c, ++q) {
+      const int s = q % R;
+      cp_async_wait<R - 1>();          // chunk q (the oldest group) has landed
+      uint4 v[VPT];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * nt;
+        v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < hv) v[k] = ld_shared_v4(slot_addr(s, k));
+      }
+      if (c < W) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) add8(acc[k], v[k]);
+        // The adds consumed the slot's values: refill it.
+        issue_next(s);
+      } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) rv[k] = v[k];
+        res_slot = s;
+      }
+    }
+    if (row + gridDim.x >= p.T) pdl_trigger();
+
+    uint4 ro[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) {
+        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        uint32_t red[4], out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
+          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+          out[e] = pack_bf16x2(s0, s1);
+          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+          ss = fmaf(q0, q0, ss);
+          ss = fmaf(q1, q1, ss);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                  make_uint4(red[0], red[1], red[2], red[3]));
+        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+      }
+    }
+    // The residual's slot is free once its values were used above.
+    issue_next(res_slot);
+    ss = warp_sum(ss);
+    float* ws = warp_ss[it & 1];
+    if (lane == 0) ws[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += ws[w];
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) {
+        const uint32_t qv[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
+        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint32_t n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n0 = (bf_lo(qv[e]) * rstd) * bf_lo(w[e]);
+          const float n1 = (bf_hi(qv[e]) * rstd) * bf_hi(w[e]);
+          n[e] = pack_bf16x2(n0, n1);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                  make_uint4(n[0], n[1], n[2], n[3]));
+      }
+    }
+  }
+  cp_async_wait<0>();   // nothing may land after the CTA exits
+}
+
 }  // namespace farn

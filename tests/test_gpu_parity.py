@@ -121,6 +121,7 @@ def _variant_outputs(dev, p, ctx):
     dict(FARN_VARIANT="cluster", FARN_CLUSTER=8), dict(FARN_VARIANT="cluster", FARN_CLUSTER=16),
     dict(FARN_VARIANT="row", FARN_VPT=1), dict(FARN_VARIANT="row", FARN_VPT=2),
     dict(FARN_VARIANT="row", FARN_VPT=4), dict(FARN_VARIANT="bulk"),
+    dict(FARN_VARIANT="stage"), dict(FARN_VARIANT="stage", FARN_STAGE_R=8),
 ], ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
 @pytest.mark.parametrize("shape", [(8, 5, 4096), (4, 37, 5120), (16, 3, 7168)],
                          ids=lambda s: f"W{s[0]}T{s[1]}H{s[2]}")
@@ -167,15 +168,66 @@ def test_bulk_variant(O, dev, name, T):
         ctx.close()
 
 
-def test_bulk_full_size_sampled(O, dev):
-    ctx = make_ctx(FARN_VARIANT="bulk")
+@pytest.mark.parametrize("env", [dict(), dict(FARN_STAGE_R=8), dict(FARN_STAGE_CTAS=2),
+                                 dict(FARN_VPT=2)],
+                         ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()) or "auto")
+@pytest.mark.parametrize("name,T", [("prefill", 1000), ("nonpow2", 613), ("wide", 300),
+                                    ("decode", 4096), ("c1", 777)])
+def test_stage_variant(O, dev, name, T, env):
+    """The cp.async-staged persistent kernel: CTAs loop over many rows and
+    each thread's slot ring wraps across row boundaries."""
+    ctx = make_ctx(FARN_VARIANT="stage", **env)
     try:
-        p = synth.workload("prefill")[0]
-        run_and_check(O, p, dev, ctx=ctx, rows=sample_rows(p.T, 96, seed=5))
-        assert farn.farn_device_status(ctx.handle) == 0
+        p = synth.workload(name)[0].with_T(T)
+        xs, res, w = synth.device_inputs(p, dev)
+        outs = [torch.empty_like(res) for _ in range(3)]
+        args = (ctx.handle, p.W, p.T, p.H, [x.data_ptr() for x in xs], res.data_ptr(),
+                w.data_ptr(), *[o.data_ptr() for o in outs])
+        t4 = (p.H // 8 // 4 + 31) // 32 * 32          # threads at 4 and 2 vectors
+        t2 = (p.H // 8 // 2 + 31) // 32 * 32
+        budget = 232448 // 2 - 1024
+        if env.get("FARN_STAGE_CTAS") == 2 and 8 * 4 * t4 * 16 > budget \
+                and 8 * 2 * t2 * 16 > budget:
+            # even 8 chunks in flight do not fit two CTAs per SM: refused
+            with pytest.raises(farn.FarnError) as e:
+                farn.farn_plan(*args)
+            assert e.value.status == farn.FARN_ERR_UNSUPPORTED
+            return
+        assert farn.farn_plan(*args)[0] == "stage"
+        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx)
+        torch.cuda.synchronize()
+        assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, p.eps),
+                      f"stage {name} T={T} {env}")
     finally:
         ctx.close()
-        torch.cuda.empty_cache()
+
+
+def test_stage_in_place_and_few_rows(O, dev):
+    """Fewer rows than CTAs (T < grid) and an in-place residual update."""
+    ctx = make_ctx(FARN_VARIANT="stage")
+    try:
+        for T in (1, 3, 151):
+            xs, res, w = _inputs(dev, 8, T, 8192, seed=T)
+            want = oracle_rows(O, xs, res, w, 1e-6)
+            red, nrm = torch.empty_like(res), torch.empty_like(res)
+            farn.forward(xs, res, w, 1e-6, out=(red, res, nrm), ctx=ctx)
+            torch.cuda.synchronize()
+            assert_parity([u16(red), u16(res), u16(nrm)], want, f"stage in place T={T}")
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("variant", ["bulk", "stage"])
+def test_persistent_variants_full_size_sampled(O, dev, variant):
+    ctx = make_ctx(FARN_VARIANT=variant)
+    try:
+        for name in ("prefill", "wide"):
+            p = synth.workload(name)[0]
+            run_and_check(O, p, dev, ctx=ctx, rows=sample_rows(p.T, 96, seed=5))
+            assert farn.farn_device_status(ctx.handle) == 0
+            torch.cuda.empty_cache()
+    finally:
+        ctx.close()
 
 
 def test_plan_choices(dev):
@@ -187,7 +239,9 @@ def test_plan_choices(dev):
             g = 1 << 32
             return farn.farn_plan(c.handle, W, T, H, [a] * W, a + g, a + 2 * g,
                                   a + 3 * g, a + 4 * g, a + 5 * g)
-        assert plan(8, 8192, 8192)[0] == "row"
+        assert plan(8, 8192, 8192) == ("stage", 1, 512)  # 2 vectors/thread, 1 CTA/SM
+        assert plan(16, 4096, 7168) == ("stage", 1, 224)  # 4 vectors/thread, 2 CTAs/SM
+        assert plan(4, 32768, 5120) == ("stage", 1, 160)
         assert plan(8, 1, 4096)[0] == "cluster"
         assert plan(8, 1, 4096)[1] == 8
         assert plan(8, 64, 4096) == ("row", 1, 512)     # decode: all ranks at once
