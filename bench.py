@@ -443,7 +443,8 @@ def run_gpu(args):
         c["variant"] = f"{v} cluster={cs} threads={thr}"
     dom = max(per_call, key=lambda c: c["kernel_us"] * c["count_per_step"])
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
-                "frac": dom["frac"], "traffic": None,
+                "frac": dom["frac"], "traffic": measured_traffic(dom["call"], dom["variant"]),
+                "kernel_source_sha": kernel_source_sha(),
                 "kernel": kernel_name(dom["variant"]), "call": dom["call"],
                 "algorithmic_bytes_per_launch": dom["bytes"],
                 "launch_us": dom["kernel_us"],
@@ -493,8 +494,47 @@ def run_gpu(args):
     return 0
 
 
+KERNELS = {"row": "farn_vec_kernel", "cluster": "farn_vec_kernel",
+           "generic": "farn_generic_kernel", "bulk": "farn_bulk_kernel",
+           "stage": "farn_stage_kernel"}
+KERNEL_SOURCES = ("rank_sum_residual_gb300/csrc/farn_kernels.cuh",
+                  "rank_sum_residual_gb300/csrc/farn.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+
+
 def kernel_name(variant):
-    return "farn_vec_kernel" if not variant.startswith("generic") else "farn_generic_kernel"
+    return KERNELS[variant.split()[0]]
+
+
+def kernel_source_sha() -> str:
+    """Hash of the kernel and launch-plan sources: ncu counters taken with
+    another hash describe another kernel."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(call: str, variant: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    of this call from the committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            lines = fh.read().splitlines()
+    except OSError:
+        return None
+    sha = kernel_source_sha()
+    key = variant.replace(" ", "_")
+    for line in lines:
+        if not line.startswith("traffic "):
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split()[1:])
+        if f.get("call") == call and f.get("plan") == key and f.get("sha") == sha:
+            return int(f["bytes"])
+    return None
 
 
 def plan_args(call):
