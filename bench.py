@@ -57,7 +57,9 @@ def parse_args(argv=None):
                     help="timed steps (default: about 1.5 s of GPU time)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=["decode", "c1", "prefill", "nonpow2", "wide"])
+                    choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm"])
+    ap.add_argument("--in-place", action="store_true",
+                    help="write residual_out over the residual (in-place residual update)")
     ap.add_argument("--impl", default="farn", choices=["farn", "reference"])
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each call from Python instead of replaying a CUDA graph")
@@ -353,6 +355,11 @@ def run_gpu(args):
                 xs, res, w = synth.device_inputs(p, dev, seed=p.seed + 7919 * k)
                 outs = tuple(torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev)
                              for _ in range(3))
+                if args.in_place:
+                    # residual_out is the residual buffer itself; every step
+                    # then reads the residual the previous step over that
+                    # copy wrote, which leaves the bytes moved unchanged
+                    outs = (outs[0], res, outs[2])
                 calls.append((p, xs, res, w, outs))
             sets.append(calls)
     stream.synchronize()
@@ -373,24 +380,39 @@ def run_gpu(args):
     # ---- CUDA graph: one replay is one rotation, i.e. one step over every
     # input copy in turn (n_sets steps), so the host issues one replay per
     # n_sets steps and never paces the GPU.
+    # Plus one graph per copy (one step each) for step counts that are not
+    # whole rotations: exactly the requested number of steps is run.
     use_graph = not args.no_graph
-    graph = None
+    graph, step_graphs = None, []
     if use_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for k in range(n_sets):
                 step(k)
+        for k in range(n_sets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(k)
+            step_graphs.append(g)
         graph.replay()
+        for g in step_graphs:
+            g.replay()
         stream.synchronize()
+    pos = [0]          # input copy the next step uses
 
     def run_steps(n):
-        """n steps (a multiple of n_sets when graphs are used)."""
-        if use_graph:
-            for _ in range(n // n_sets):
+        """Exactly n steps, continuing the rotation over the input copies."""
+        while n > 0:
+            if use_graph and pos[0] == 0 and n >= n_sets:
                 graph.replay()
-        else:
-            for i in range(n):
-                step(i % n_sets)
+                n -= n_sets
+                continue
+            if use_graph:
+                step_graphs[pos[0]].replay()
+            else:
+                step(pos[0])
+            pos[0] = (pos[0] + 1) % n_sets
+            n -= 1
 
     # ---- step count: about 1.5 s of GPU time unless given
     K = args.steps
@@ -402,13 +424,11 @@ def run_gpu(args):
     calib_ms = e0.elapsed_time(e1) / (4 * n_sets)
     if K is None:
         K = max(20, int(1500.0 / max(calib_ms, 1e-4)))
-    if use_graph:
-        K = max(n_sets, (K + n_sets - 1) // n_sets * n_sets)
+        K = (K + n_sets - 1) // n_sets * n_sets
 
     sampler = ClockSampler(gpu_id_for(local)).start() if rank == 0 else None
     time.sleep(0.5 if sampler else 0)
-    run_steps(max(args.warmup, 1) if not use_graph else
-              max(n_sets, (args.warmup + n_sets - 1) // n_sets * n_sets))
+    run_steps(args.warmup)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
@@ -471,10 +491,12 @@ def run_gpu(args):
                        "calls_per_step": len(problems), "rows_per_step": step_rows,
                        "bytes_per_step": step_bytes,
                        "accumulate": "f32",
+                       "residual_out": "in place over residual" if args.in_place else "separate",
                        "l2": f"inputs rotated over {n_sets} device copies "
                              f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB); "
                              "no flush",
-                       "launch": (f"CUDA graph, one replay per {n_sets} steps"
+                       "launch": (f"CUDA graphs: one replay per rotation of {n_sets} "
+                                  "input copies, one-step graphs for the rest"
                                   if use_graph else "direct launches"),
                        "calibration_ms_per_step": calib_ms,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -67,6 +67,14 @@ def _declare(lib):
                                    u16p, ctypes.c_float, ctypes.c_int64,
                                    ctypes.c_int64, u16p, u16p, u16p]
     lib.oracle_forward.restype = ctypes.c_int
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_rank_sum_f32.argtypes = [ctypes.POINTER(f32p), ctypes.c_int,
+                                        ctypes.c_int64, u16p]
+    lib.oracle_rank_sum_f32.restype = None
+    lib.oracle_forward_f32.argtypes = [ctypes.POINTER(f32p), ctypes.c_int, u16p,
+                                       u16p, ctypes.c_float, ctypes.c_int64,
+                                       ctypes.c_int64, u16p, u16p, u16p]
+    lib.oracle_forward_f32.restype = ctypes.c_int
     return lib
 
 
@@ -93,6 +101,10 @@ def _p(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16))
 
 
+def _pf(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
 class Oracle:
     """numpy front end over one loaded oracle library."""
 
@@ -109,6 +121,12 @@ class Oracle:
         return int(self.lib.oracle_f32_bits_to_bf16(int(u) & 0xFFFFFFFF))
 
     def rank_sum(self, xs) -> np.ndarray:
+        if np.asarray(xs[0]).dtype == np.float32:
+            xs = [np.ascontiguousarray(x, dtype=np.float32) for x in xs]
+            out = np.empty(xs[0].shape, np.uint16)
+            arr = (ctypes.POINTER(ctypes.c_float) * len(xs))(*[_pf(x) for x in xs])
+            self.lib.oracle_rank_sum_f32(arr, len(xs), xs[0].size, _p(out))
+            return out
         xs = [_u16(x) for x in xs]
         n = xs[0].size
         out = np.empty(xs[0].shape, np.uint16)
@@ -131,8 +149,12 @@ class Oracle:
         return out, float(rstd)
 
     def forward(self, xs, residual, weight, eps: float):
-        """All three outputs for W partials [T,H], residual [T,H], weight [H]."""
-        xs = [_u16(x) for x in xs]
+        """All three outputs for W partials [T,H], residual [T,H], weight [H].
+
+        Partials are bf16 patterns (uint16) or fp32 (float32) arrays."""
+        f32 = np.asarray(xs[0]).dtype == np.float32
+        xs = [np.ascontiguousarray(x, dtype=np.float32) for x in xs] if f32 \
+            else [_u16(x) for x in xs]
         residual, weight = _u16(residual), _u16(weight)
         if residual.ndim != 2:
             raise ValueError("residual must be [T, H]")
@@ -145,9 +167,14 @@ class Oracle:
         reduced = np.empty((T, H), np.uint16)
         ro = np.empty((T, H), np.uint16)
         norm = np.empty((T, H), np.uint16)
-        arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x) for x in xs])
-        rc = self.lib.oracle_forward(arr, len(xs), _p(residual), _p(weight),
-                                     eps, T, H, _p(reduced), _p(ro), _p(norm))
+        if f32:
+            arr = (ctypes.POINTER(ctypes.c_float) * len(xs))(*[_pf(x) for x in xs])
+            rc = self.lib.oracle_forward_f32(arr, len(xs), _p(residual), _p(weight),
+                                             eps, T, H, _p(reduced), _p(ro), _p(norm))
+        else:
+            arr = (ctypes.POINTER(ctypes.c_uint16) * len(xs))(*[_p(x) for x in xs])
+            rc = self.lib.oracle_forward(arr, len(xs), _p(residual), _p(weight),
+                                         eps, T, H, _p(reduced), _p(ro), _p(norm))
         if rc != 0:
             raise ValueError(f"oracle_forward rejected its arguments (rc={rc})")
         return reduced, ro, norm

@@ -134,6 +134,23 @@ float oracle_rmsnorm_row(const uint16_t *ro, const uint16_t *weight,
     return rstd;
 }
 
+/* Step a1 with fp32 partials (the partial sums of a GEMM epilogue, say):
+ * the same rank-order FP32 sum, the partials' own fp32 values used as they
+ * are (no rounding to bf16 before the sum), the sum rounded once to bf16. */
+static uint16_t rank_sum_one_f32(const float *const *x, int W, int64_t idx)
+{
+    float acc = x[0][idx];
+    for (int r = 1; r < W; ++r)
+        acc = acc + x[r][idx];
+    return oracle_f32_to_bf16(acc);
+}
+
+void oracle_rank_sum_f32(const float *const *x, int W, int64_t n, uint16_t *reduced)
+{
+    for (int64_t i = 0; i < n; ++i)
+        reduced[i] = rank_sum_one_f32(x, W, i);
+}
+
 /* The whole operator on row-major [T,H] tensors, row after row, in the
  * order of the contract: rank sum, residual add, RMSNorm.
  * x is an array of W pointers, one per rank partial.  Returns 0, or -1 on
@@ -157,6 +174,31 @@ int oracle_forward(const uint16_t *const *x, int W, const uint16_t *residual,
         for (int r = 0; r < W; ++r)
             row_x[r] = x[r] + off;
         oracle_rank_sum(row_x, W, H, reduced + off);
+        oracle_residual_add(reduced + off, residual + off, H, residual_out + off);
+        oracle_rmsnorm_row(residual_out + off, weight, eps, H, norm_out + off);
+    }
+    return 0;
+}
+
+/* The whole operator with fp32 partials; residual, weight and the three
+ * outputs bf16 as in oracle_forward.  Same return convention. */
+int oracle_forward_f32(const float *const *x, int W, const uint16_t *residual,
+                       const uint16_t *weight, float eps, int64_t T, int64_t H,
+                       uint16_t *reduced, uint16_t *residual_out,
+                       uint16_t *norm_out)
+{
+    if (W < 1 || W > 256 || T < 0 || H < 1 || !x || !residual || !weight ||
+        !reduced || !residual_out || !norm_out)
+        return -1;
+    for (int r = 0; r < W; ++r)
+        if (!x[r])
+            return -1;
+    const float *row_x[256];
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t off = t * H;
+        for (int r = 0; r < W; ++r)
+            row_x[r] = x[r] + off;
+        oracle_rank_sum_f32(row_x, W, H, reduced + off);
         oracle_residual_add(reduced + off, residual + off, H, residual_out + off);
         oracle_rmsnorm_row(residual_out + off, weight, eps, H, norm_out + off);
     }

@@ -99,6 +99,8 @@ WORKLOADS = {
                         N01, Dist(UNIFORM, 0.5, 1.5))],
     "nonpow2": [Problem("nonpow2", 4, 32768, 5120, 1e-6, 0, N01)],
     "wide": [Problem("wide", 16, 4096, 7168, 1e-6, 0, Dist(NORMAL, 0.0, 1.0 / 16))],
+    # residual add + RMSNorm alone (one partial: no rank sum), prefill-sized
+    "rmsnorm": [Problem("rmsnorm", 1, 8192, 8192, 1e-6, 0, N01)],
 }
 
 

@@ -19,8 +19,9 @@ import numpy as np
 
 import bf16_exact as bx
 
-GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
-                      "hand_rows.txt")
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+GOLDEN = os.path.join(GOLDEN_DIR, "hand_rows.txt")
+GOLDEN_F32 = os.path.join(GOLDEN_DIR, "hand_rows_f32.txt")
 
 
 # ------------------------------------------------------------------- goldens
@@ -51,12 +52,23 @@ def _compare(name, key, got, want):
     assert ok.all(), f"{name}.{key}: got {[hex(v) for v in got]} want {[hex(v) for v in want]}"
 
 
-def pin_golden_cases(O):
-    for name, c in load_golden().items():
+def _row_f32(s: str) -> np.ndarray:
+    vals = []
+    for t in s.split():
+        q = Fraction(t)
+        f = np.float32(float(q))
+        assert Fraction(float(f)) == q, f"{t} is not exact in fp32"
+        vals.append(f)
+    return np.array(vals, np.float32)
+
+
+def pin_golden_cases(O, path=GOLDEN):
+    for name, c in load_golden(path).items():
         xs = []
         r = 0
+        f32 = c.get("partial_dtype") == "f32"
         while f"x{r}" in c:
-            xs.append(_row(c[f"x{r}"])[None, :])
+            xs.append((_row_f32 if f32 else _row)(c[f"x{r}"])[None, :])
             r += 1
         res = _row(c["residual"])[None, :]
         w = _row(c["weight"])
@@ -282,6 +294,67 @@ def pin_row_tiling_independent(O):
         nrm, _ = O.rmsnorm_row(ro, w, 1e-6)
         assert np.array_equal(red, full[0][t]) and np.array_equal(ro, full[1][t])
         assert np.array_equal(nrm, full[2][t])
+
+
+# ------------------------------------------------------- fp32 partials (a1)
+def pin_golden_cases_f32_partials(O):
+    pin_golden_cases(O, GOLDEN_F32)
+
+
+def pin_rank_sum_f32_integers(O):
+    """Integer-valued fp32 partials (|x| <= 2^18, W <= 32: every prefix sum
+    exact in fp32): the exact integer sum rounded once to bf16."""
+    rng = np.random.default_rng(17)
+    for W in (1, 2, 5, 16, 32):
+        vals = rng.integers(-(1 << 18), (1 << 18) + 1, size=(W, 301))
+        xs = [v.astype(np.float32) for v in vals]
+        got = O.rank_sum(xs)
+        want = [bx.round_rne(Fraction(int(t))) if t != 0 else 0 for t in vals.sum(axis=0)]
+        assert list(got) == want, f"W={W}"
+
+
+def pin_rank_sum_f32_brute_force(O):
+    """fp32 partials of mixed magnitude against the exact rational sum: equal
+    where every prefix is exact in fp32, within 1 ulp elsewhere."""
+    rng = np.random.default_rng(19)
+    n_exact = 0
+    for W in (2, 3, 4):
+        # 12 significant bits, so that many (not all) prefix sums are exact
+        m = np.round(rng.normal(size=(W, 500)) * 2048) / 2048
+        xs = [(mi * np.exp2(rng.integers(-10, 10, 500))).astype(np.float32) for mi in m]
+        got = O.rank_sum(xs)
+        for i in range(got.size):
+            terms = [Fraction(float(x[i])) for x in xs]
+            prefix, exact = terms[0], True
+            for t in terms[1:]:
+                prefix += t
+                exact &= _fp32_exact(prefix)
+            if prefix == 0:
+                assert (int(got[i]) & 0x7FFF) == 0
+                continue
+            want = bx.round_rne(prefix)
+            if exact:
+                n_exact += 1
+                assert int(got[i]) == want, (W, i, hex(int(got[i])), hex(want))
+            else:
+                assert bx.ulp_diff(int(got[i]), want) <= 1
+    assert n_exact > 200
+
+
+def pin_f32_partials_equal_bf16_path_on_bf16_values(O):
+    """fp32 partials that hold bf16 values give exactly the bf16 path's
+    outputs (same fp32 arithmetic on the same values)."""
+    rng = np.random.default_rng(23)
+    T, H, W = 5, 96, 6
+    xb = [(rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(W)]
+    xf = [bx.to_f64(x).astype(np.float32) for x in xb]
+    res = (rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = (rng.normal(1, .1, H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    a = O.forward(xb, res, w, 1e-6)
+    b = O.forward(xf, res, w, 1e-6)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

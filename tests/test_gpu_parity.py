@@ -97,7 +97,7 @@ def test_mid_size_full(O, dev, name, T):
     run_and_check(O, synth.workload(name)[0].with_T(T), dev)
 
 
-@pytest.mark.parametrize("name", ["prefill", "nonpow2", "wide"])
+@pytest.mark.parametrize("name", ["prefill", "nonpow2", "wide", "rmsnorm"])
 def test_full_size_sampled_rows(O, dev, name):
     """Full benchmark size, default launch plan (as the benchmark times it);
     the oracle recomputes 160 sampled rows (first, middle, last, random)."""
@@ -481,3 +481,21 @@ def test_bulk_forced_on_unsupported_shape_is_an_error(dev):
         assert e.value.status == farn.FARN_ERR_UNSUPPORTED
     finally:
         ctx.close()
+
+
+@pytest.mark.parametrize("name", ["rmsnorm", "prefill"])
+def test_full_size_in_place(O, dev, name):
+    """residual_out written over the residual at full size, default plan."""
+    p = synth.workload(name)[0]
+    xs, res, w = synth.device_inputs(p, dev)
+    rows = sample_rows(p.T, 96, seed=11)
+    idx = torch.as_tensor(rows, device=dev)
+    want = O.forward([u16(x.index_select(0, idx)) for x in xs],
+                     u16(res.index_select(0, idx)), u16(w), p.eps)
+    red, nrm = torch.empty_like(res), torch.empty_like(res)
+    farn.forward(xs, res, w, p.eps, out=(red, res, nrm))
+    torch.cuda.synchronize()
+    got = [u16(t.index_select(0, idx)) for t in (red, res, nrm)]
+    assert_parity(got, want, f"{name} in place")
+    del xs, res, w, red, nrm
+    torch.cuda.empty_cache()

@@ -47,7 +47,19 @@ MUTANTS = {
     "divide_instead_of_multiply": (
         "float n = v * rstd;", "float n = v / rstd;"),
     "row_offset_wrong": (
-        "int64_t off = t * H;", "int64_t off = t * (H - 1);"),
+        "int64_t off = t * H;\n        for (int r = 0; r < W; ++r)\n            row_x[r] = x[r] + off;\n        oracle_rank_sum(row_x",
+        "int64_t off = t * (H - 1);\n        for (int r = 0; r < W; ++r)\n            row_x[r] = x[r] + off;\n        oracle_rank_sum(row_x"),
+    "f32_partials_prerounded": (
+        "acc = acc + x[r][idx];",
+        "acc = acc + oracle_bf16_to_f32(oracle_f32_to_bf16(x[r][idx]));"),
+    "f32_reverse_rank_order": (
+        "for (int r = 1; r < W; ++r)\n        acc = acc + x[r][idx];",
+        "for (int r = W - 1; r >= 1; --r)\n        acc = acc + x[r][idx];"),
+    "f32_first_partial_dropped": (
+        "float acc = x[0][idx];", "float acc = 0.0f * x[0][idx];"),
+    "f32_row_offset_wrong": (
+        "            row_x[r] = x[r] + off;\n        oracle_rank_sum_f32",
+        "            row_x[r] = x[r] + off / 2;\n        oracle_rank_sum_f32"),
     "widen_drops_low_bit": (
         "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)(b & 0xFFFEu)) << 16;"),
 }
