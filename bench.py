@@ -57,7 +57,8 @@ def parse_args(argv=None):
                     help="timed steps (default: about 1.5 s of GPU time)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm"])
+                    choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm",
+                             "prefill_f32"])
     ap.add_argument("--in-place", action="store_true",
                     help="write residual_out over the residual (in-place residual update)")
     ap.add_argument("--impl", default="farn", choices=["farn", "reference"])
@@ -195,8 +196,9 @@ def gpu_id_for(dev_index):
 
 # -------------------------------------------------------- CPU (the oracle)
 def row_bytes(p) -> int:
-    """Algorithmic bytes of one row of a call (weight counted per call)."""
-    return (p.W + 4) * p.H * 2
+    """Algorithmic bytes of one row of a call (weight counted per call):
+    W partial rows of H elements, the residual row, three output rows."""
+    return p.W * p.H * p.partial_bytes + 4 * p.H * 2
 
 
 def call_bytes(p, rows) -> int:
@@ -459,7 +461,7 @@ def run_gpu(args):
     for j, c in enumerate(per_call):
         c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
         c["frac"] = c["gbs"] / peak
-        v, cs, thr = farn.farn_plan(ctx.handle, *plan_args(sets[0][j]))
+        v, cs, thr = farn.farn_plan_typed(ctx.handle, *plan_args(sets[0][j]))
         c["variant"] = f"{v} cluster={cs} threads={thr}"
     dom = max(per_call, key=lambda c: c["kernel_us"] * c["count_per_step"])
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
@@ -519,8 +521,7 @@ def run_gpu(args):
 KERNELS = {"row": "farn_vec_kernel", "cluster": "farn_vec_kernel",
            "generic": "farn_generic_kernel", "bulk": "farn_bulk_kernel",
            "stage": "farn_stage_kernel"}
-KERNEL_SOURCES = ("rank_sum_residual_gb300/csrc/farn_kernels.cuh",
-                  "rank_sum_residual_gb300/csrc/farn.cu")
+KERNEL_SOURCES = ("rank_sum_residual_gb300/csrc/farn_kernels.cuh",)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
 
@@ -529,8 +530,8 @@ def kernel_name(variant):
 
 
 def kernel_source_sha() -> str:
-    """Hash of the kernel and launch-plan sources: ncu counters taken with
-    another hash describe another kernel."""
+    """Hash of the kernel source: ncu counters taken with another hash
+    describe another kernel."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -560,8 +561,10 @@ def measured_traffic(call: str, variant: str):
 
 
 def plan_args(call):
+    import rank_sum_residual_gb300 as farn
     p, xs, res, w, outs = call
-    return (p.W, p.T, p.H, [x.data_ptr() for x in xs], res.data_ptr(), w.data_ptr(),
+    return (farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16, p.W, p.T, p.H,
+            [x.data_ptr() for x in xs], res.data_ptr(), w.data_ptr(),
             outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr())
 
 
@@ -576,8 +579,8 @@ def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
     out = []
     for p in problems:
         copies = max(2, math.ceil(2 * l2_bytes / p.algorithmic_bytes()))
-        xs = [torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
-              for _ in range(p.W)]
+        xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
+        xs = [torch.empty((copies, p.T, p.H), dtype=xdt, device=dev) for _ in range(p.W)]
         res = torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
         w = torch.empty((p.H,), dtype=torch.bfloat16, device=dev)
         for r, x in enumerate(xs):
@@ -621,29 +624,35 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     import torch
     import rank_sum_residual_gb300 as farn
 
-    in_elems = sum((p.W + 1) * p.T * p.H + p.H for p in problems)
+    # inputs packed as bytes (partials may be fp32), outputs bf16
+    in_bytes = sum(p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
+                   for p in problems)
     out_elems = sum(3 * p.T * p.H for p in problems)
-    host_in = torch.empty(in_elems, dtype=torch.bfloat16).pin_memory()
+    host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
     host_out = [torch.empty(out_elems, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     off = 0
     for p, xs, res, w, outs in calls:          # the step's inputs, packed
         for t in (*xs, res, w):
-            n = t.numel()
-            host_in[off:off + n].copy_(t.reshape(-1))
-            off += n
+            b = t.reshape(-1).view(torch.uint8)
+            host_in[off:off + b.numel()].copy_(b)
+            off += b.numel()
     slots = []
     for _ in range(2):
-        dev_in = torch.empty(in_elems, dtype=torch.bfloat16, device=dev)
+        dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
         dev_out = torch.empty(out_elems, dtype=torch.bfloat16, device=dev)
         views, oi, oo = [], 0, 0
+
+        def take(nbytes, dtype, shape):
+            nonlocal oi
+            t = dev_in[oi:oi + nbytes].view(dtype).view(*shape)
+            oi += nbytes
+            return t
         for p in problems:
             n = p.T * p.H
-            xs = [dev_in[oi + r * n: oi + (r + 1) * n].view(p.T, p.H) for r in range(p.W)]
-            oi += p.W * n
-            res = dev_in[oi:oi + n].view(p.T, p.H)
-            oi += n
-            w = dev_in[oi:oi + p.H]
-            oi += p.H
+            xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
+            xs = [take(n * p.partial_bytes, xdt, (p.T, p.H)) for _ in range(p.W)]
+            res = take(n * 2, torch.bfloat16, (p.T, p.H))
+            w = take(p.H * 2, torch.bfloat16, (p.H,))
             outs = tuple(dev_out[oo + k * n: oo + (k + 1) * n].view(p.T, p.H) for k in range(3))
             oo += 3 * n
             views.append((p, xs, res, w, outs))
@@ -696,7 +705,7 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     # the last step's outputs really came back
     assert torch.equal(host_out[(Ke - 1) % 2][-8:], slots[(Ke - 1) % 2][1][-8:].cpu())
     return {"value": world * step_bytes * Ke / (ms / 1e3) / 1e9, "unit": UNIT,
-            "h2d_bytes_per_step": in_elems * 2, "d2h_bytes_per_step": out_elems * 2,
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_elems * 2,
             "steps": Ke, "ms_per_step": ms / Ke,
             "path": "per step: one pinned-host -> device copy of all inputs, "
                     "farn_forward for every call (C ABI via the Python binding), one "

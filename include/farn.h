@@ -59,6 +59,12 @@ typedef enum {
     FARN_ERR_NOMEM = -5         /* host allocation of the context failed     */
 } farn_status;
 
+/* Element types of the partials (farn_forward_typed). */
+typedef enum {
+    FARN_BF16 = 0,   /* bfloat16, 2 bytes */
+    FARN_F32 = 1     /* IEEE binary32, 4 bytes */
+} farn_dtype;
+
 /* Opaque per-device context: device properties and kernel attributes
  * queried once.  Immutable after farn_create; one context may serve any
  * number of streams and host threads at once. */
@@ -100,6 +106,22 @@ int farn_forward(const farn_ctx *ctx,
                  int64_t T, int64_t H,
                  void *reduced_out, void *residual_out, void *norm_out,
                  cudaStream_t stream);
+
+/* farn_forward with the partials in `partial_dtype` (a farn_dtype):
+ * FARN_BF16 is exactly farn_forward; FARN_F32 takes fp32 partials [T,H]
+ * (for example the fp32 output of a GEMM epilogue, before any rounding)
+ * and sums their own fp32 values in rank order, rounding once to bf16 --
+ * the "FP32 accumulation where required" of the page's Implementation
+ * section 3.  residual, weight and the three outputs stay bf16; everything
+ * else (layout, ownership, aliasing, errors) is as for farn_forward, with
+ * each fp32 partial occupying T*H*4 bytes.  Returns FARN_ERR_INVALID_ARG
+ * for an unknown dtype. */
+int farn_forward_typed(const farn_ctx *ctx,
+                       const void *const *partials, int partial_dtype, int W,
+                       const void *residual, const void *weight, float eps,
+                       int64_t T, int64_t H,
+                       void *reduced_out, void *residual_out, void *norm_out,
+                       cudaStream_t stream);
 
 /* The argument checks of farn_forward alone, on the host: no CUDA call, no
  * launch, pointers are only compared, never dereferenced.  Returns what
@@ -176,6 +198,14 @@ int farn_forward_noalloc(int device,
                          int64_t T, int64_t H,
                          void *reduced_out, void *residual_out, void *norm_out,
                          cudaStream_t stream, int *status_out);
+
+/* farn_plan for partials of type `partial_dtype` (a farn_dtype); fp32
+ * partials are sized T*H*4 bytes in the aliasing checks. */
+int farn_plan_typed(const farn_ctx *ctx, int partial_dtype, int W, int64_t T, int64_t H,
+                    const void *const *partials, const void *residual,
+                    const void *weight, const void *reduced_out,
+                    const void *residual_out, const void *norm_out,
+                    int *variant, int *cluster_size, int *threads);
 
 #ifdef __cplusplus
 }

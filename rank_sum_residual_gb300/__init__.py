@@ -24,6 +24,7 @@ __all__ = [
     "FARN_MAX_W", "FarnError", "Context", "build_library", "library_path",
     "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
     "farn_plan", "farn_status_string", "farn_device_status", "farn_forward_noalloc",
+    "farn_forward_typed", "farn_plan_typed", "FARN_BF16", "FARN_F32",
     "forward", "VARIANTS",
 ]
 
@@ -35,6 +36,7 @@ FARN_ERR_ALIAS = -3
 FARN_ERR_CUDA = -4
 FARN_ERR_NOMEM = -5
 VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk", 4: "stage"}
+FARN_BF16, FARN_F32 = 0, 1
 
 _lib = None
 
@@ -61,6 +63,9 @@ def _load():
         lib.farn_forward.argtypes = [vp, pvp, i32, cvp, cvp, f32, i64, i64,
                                      vp, vp, vp, vp]
         lib.farn_forward.restype = i32
+        lib.farn_forward_typed.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64,
+                                           vp, vp, vp, vp]
+        lib.farn_forward_typed.restype = i32
         lib.farn_check_args.argtypes = [pvp, i32, cvp, cvp, f32, i64, i64,
                                         cvp, cvp, cvp]
         lib.farn_check_args.restype = i32
@@ -68,6 +73,10 @@ def _load():
                                   cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                   ctypes.POINTER(i32)]
         lib.farn_plan.restype = i32
+        lib.farn_plan_typed.argtypes = [vp, i32, i32, i64, i64, pvp, cvp, cvp, cvp, cvp,
+                                        cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                        ctypes.POINTER(i32)]
+        lib.farn_plan_typed.restype = i32
         lib.farn_forward_noalloc.argtypes = [i32, pvp, i32, cvp, cvp, f32, i64, i64,
                                              vp, vp, vp, vp, ctypes.POINTER(i32)]
         lib.farn_forward_noalloc.restype = i32
@@ -112,6 +121,17 @@ def farn_forward(ctx, partials, W, residual, weight, eps, T, H,
     return _load().farn_forward(
         ctypes.c_void_p(ctx) if ctx else None, _ptr_array(partials), int(W),
         ctypes.c_void_p(int(residual)), ctypes.c_void_p(int(weight)), float(eps),
+        int(T), int(H), ctypes.c_void_p(int(reduced_out)),
+        ctypes.c_void_p(int(residual_out)), ctypes.c_void_p(int(norm_out)),
+        ctypes.c_void_p(int(stream)))
+
+
+def farn_forward_typed(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                       reduced_out, residual_out, norm_out, stream=0) -> int:
+    """C ``farn_forward_typed``: partials of dtype FARN_BF16 or FARN_F32."""
+    return _load().farn_forward_typed(
+        ctypes.c_void_p(ctx) if ctx else None, _ptr_array(partials), int(partial_dtype),
+        int(W), ctypes.c_void_p(int(residual)), ctypes.c_void_p(int(weight)), float(eps),
         int(T), int(H), ctypes.c_void_p(int(reduced_out)),
         ctypes.c_void_p(int(residual_out)), ctypes.c_void_p(int(norm_out)),
         ctypes.c_void_p(int(stream)))
@@ -168,6 +188,20 @@ def farn_plan(ctx, W, T, H, partials, residual, weight, reduced_out,
     return VARIANTS[variant.value], cs.value, thr.value
 
 
+def farn_plan_typed(ctx, partial_dtype, W, T, H, partials, residual, weight, reduced_out,
+                    residual_out, norm_out):
+    """C ``farn_plan_typed``: (variant name, CTAs per row, threads per CTA)."""
+    variant, cs, thr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    st = _load().farn_plan_typed(ctypes.c_void_p(ctx), int(partial_dtype), int(W), int(T),
+                                 int(H), _ptr_array(partials), v(residual), v(weight),
+                                 v(reduced_out), v(residual_out), v(norm_out),
+                                 ctypes.byref(variant), ctypes.byref(cs), ctypes.byref(thr))
+    if st != FARN_OK:
+        raise FarnError(st, "farn_plan_typed")
+    return VARIANTS[variant.value], cs.value, thr.value
+
+
 class Context:
     """Owns one ``farn_ctx`` for a device (``farn_create``/``farn_destroy``)."""
 
@@ -203,12 +237,13 @@ def _context_for(device_index: int) -> Context:
     return c
 
 
-def _check_tensor(t, name, shape, device):
+def _check_tensor(t, name, shape, device, dtypes=None):
     import torch
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != torch.bfloat16:
-        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    dtypes = dtypes or (torch.bfloat16,)
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
     if not t.is_cuda or t.device != device:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
     if not t.is_contiguous():
@@ -219,9 +254,11 @@ def _check_tensor(t, name, shape, device):
 
 def forward(partials, residual, weight, eps: float, out=None, ctx=None,
             stream=None):
-    """The fused operator on torch bf16 CUDA tensors.
+    """The fused operator on torch CUDA tensors.
 
-    partials: sequence of W tensors [T,H]; residual [T,H]; weight [H].
+    partials: sequence of W tensors [T,H], all bf16 or all fp32 (fp32 partials
+    are summed as fp32, see farn_forward_typed); residual [T,H] and weight
+    [H] bf16; outputs bf16.
     out: optional (reduced, residual_out, norm_out) tensors to write
     (residual_out may be ``residual`` itself).  Runs asynchronously on
     ``stream`` (default: torch's current stream) and returns the outputs.
@@ -234,8 +271,11 @@ def forward(partials, residual, weight, eps: float, out=None, ctx=None,
         raise ValueError("residual must be [T, H]")
     T, H = residual.shape
     dev = residual.device
+    pdt = partials[0].dtype
+    if pdt not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"partials must be bfloat16 or float32, got {pdt}")
     for r, x in enumerate(partials):
-        _check_tensor(x, f"partials[{r}]", (T, H), dev)
+        _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
     _check_tensor(residual, "residual", (T, H), dev)
     _check_tensor(weight, "weight", (H,), dev)
     if out is None:
@@ -245,10 +285,11 @@ def forward(partials, residual, weight, eps: float, out=None, ctx=None,
         _check_tensor(t, name, (T, H), dev)
     c = ctx if ctx is not None else _context_for(dev.index)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = farn_forward(c.handle, [x.data_ptr() for x in partials], len(partials),
-                      residual.data_ptr(), weight.data_ptr(), eps, T, H,
-                      out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
-                      s.cuda_stream)
+    st = farn_forward_typed(c.handle, [x.data_ptr() for x in partials],
+                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
+                            residual.data_ptr(), weight.data_ptr(), eps, T, H,
+                            out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+                            s.cuda_stream)
     if st != FARN_OK:
         raise FarnError(st, "farn_forward")
     return out

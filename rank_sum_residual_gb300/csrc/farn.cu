@@ -45,8 +45,7 @@ struct farn_ctx {
   int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
   int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
   int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
-  int stage_regs4;     // registers per thread of the stage kernels, 4 / 2 vectors
-  int stage_regs2;
+  int stage_regs[2];   // registers per thread of the stage kernels [4 vectors per thread]
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
 };
@@ -54,6 +53,9 @@ struct farn_ctx {
 namespace {
 
 typedef void (*VecKernel)(const farn::Params);
+
+// Chunks in flight per thread that the stage kernels are built for.
+constexpr int kStageDepths[3] = {16, 12, 8};
 
 VecKernel pick_stage(int vpt, int r) {
   if (vpt == 2) {
@@ -68,6 +70,10 @@ VecKernel pick_stage(int vpt, int r) {
   return nullptr;
 }
 
+VecKernel pick_generic(int pb) {
+  return pb == 4 ? &farn::farn_generic_kernel<4> : &farn::farn_generic_kernel<2>;
+}
+
 VecKernel pick_bulk(int vpt) {
   switch (vpt) {
     case 1: return &farn::farn_bulk_kernel<1>;
@@ -79,6 +85,7 @@ VecKernel pick_bulk(int vpt) {
 
 struct Plan {
   int variant;
+  int pb;       // bytes per partial element
   int cs;       // CTAs per row
   int vpt;      // vectors per thread
   int threads;  // threads per CTA
@@ -119,33 +126,38 @@ bool make_bulk_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
   return true;
 }
 
-template <int VPT, int CS>
-VecKernel vec_kernel() { return &farn::farn_vec_kernel<VPT, CS>; }
+template <int VPT, int CS, int PB>
+VecKernel vec_kernel() { return &farn::farn_vec_kernel<VPT, CS, PB>; }
 
-VecKernel pick_vec(int vpt, int cs) {
+template <int PB>
+VecKernel pick_vec_pb(int vpt, int cs) {
   switch (cs) {
     case 1:
-      switch (vpt) { case 1: return vec_kernel<1, 1>(); case 2: return vec_kernel<2, 1>();
-                     case 4: return vec_kernel<4, 1>(); }
+      switch (vpt) { case 1: return vec_kernel<1, 1, PB>(); case 2: return vec_kernel<2, 1, PB>();
+                     case 4: return vec_kernel<4, 1, PB>(); }
       break;
     case 2:
-      switch (vpt) { case 1: return vec_kernel<1, 2>(); case 2: return vec_kernel<2, 2>();
-                     case 4: return vec_kernel<4, 2>(); }
+      switch (vpt) { case 1: return vec_kernel<1, 2, PB>(); case 2: return vec_kernel<2, 2, PB>();
+                     case 4: return vec_kernel<4, 2, PB>(); }
       break;
     case 4:
-      switch (vpt) { case 1: return vec_kernel<1, 4>(); case 2: return vec_kernel<2, 4>();
-                     case 4: return vec_kernel<4, 4>(); }
+      switch (vpt) { case 1: return vec_kernel<1, 4, PB>(); case 2: return vec_kernel<2, 4, PB>();
+                     case 4: return vec_kernel<4, 4, PB>(); }
       break;
     case 8:
-      switch (vpt) { case 1: return vec_kernel<1, 8>(); case 2: return vec_kernel<2, 8>();
-                     case 4: return vec_kernel<4, 8>(); }
+      switch (vpt) { case 1: return vec_kernel<1, 8, PB>(); case 2: return vec_kernel<2, 8, PB>();
+                     case 4: return vec_kernel<4, 8, PB>(); }
       break;
     case 16:
-      switch (vpt) { case 1: return vec_kernel<1, 16>(); case 2: return vec_kernel<2, 16>();
-                     case 4: return vec_kernel<4, 16>(); }
+      switch (vpt) { case 1: return vec_kernel<1, 16, PB>(); case 2: return vec_kernel<2, 16, PB>();
+                     case 4: return vec_kernel<4, 16, PB>(); }
       break;
   }
   return nullptr;
+}
+
+VecKernel pick_vec(int vpt, int cs, int pb) {
+  return pb == 4 ? pick_vec_pb<4>(vpt, cs) : pick_vec_pb<2>(vpt, cs);
 }
 
 bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
@@ -187,17 +199,18 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
   if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
   const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
   if (nt > 512) return false;
-  const int regs = vpt >= 4 ? ctx->stage_regs4 : ctx->stage_regs2;
+  const int regs = ctx->stage_regs[vpt >= 4];
   if ((int64_t)regs * nt * ctas > 65536) return false;
   const size_t budget = (size_t)ctx->max_smem / (size_t)ctas - 1024;
   int r = 0;
-  const int cand_r[3] = {16, 12, 8};
   for (int i = 0; i < 3 && !r; ++i) {
-    if (ctx->stage_r > 0 && cand_r[i] != ctx->stage_r) continue;
-    if ((size_t)cand_r[i] * vpt * nt * 16 <= budget) r = cand_r[i];
+    const int cand = kStageDepths[i];
+    if (ctx->stage_r > 0 && cand != ctx->stage_r) continue;
+    if ((size_t)cand * vpt * nt * 16 <= budget) r = cand;
   }
   if (!r || !pick_stage(vpt, r)) return false;
   pl->variant = kVariantStage;
+  pl->pb = 2;
   pl->cs = 1;
   pl->vpt = vpt;
   pl->threads = (int)nt;
@@ -208,12 +221,13 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
   return true;
 }
 
+// bf16 partials only (fp32 partials take the row kernel, see the kernel).
 bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
   const int64_t hv = H / 8;
   const int vpts[2] = {4, 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
-    return stage_fit(ctx, hv, 4, ctx->stage_ctas, pl, T) ||
-           stage_fit(ctx, hv, 2, ctx->stage_ctas, pl, T);
+    return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T) ||
+           stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T);
   for (int i = 0; i < 2; ++i) {
     const int vpt = vpts[i];
     const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
@@ -225,13 +239,14 @@ bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
   return stage_fit(ctx, hv, 2, 1, pl, T) || stage_fit(ctx, hv, 4, 1, pl, T);
 }
 
-int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
+int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out) {
   Plan pl;
+  pl.pb = pb;
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
   const bool small = T < ctx->small_t;
   pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
-  if (vec_ok && (want == kVariantBulk ||
+  if (vec_ok && pb == 2 && (want == kVariantBulk ||
                  (want == kVariantAuto && ctx->bulk && !small && ctx->force_cluster == 0)) &&
       make_bulk_plan(ctx, T, H, &pl)) {
     *out = pl;
@@ -239,7 +254,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out)
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   pl.stage_r = 0;
-  if (vec_ok && (want == kVariantStage ||
+  if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
                   ctx->force_cluster == 0)) &&
       make_stage_plan(ctx, T, H, &pl)) {
@@ -280,7 +295,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out)
       *out = pl;
       return FARN_OK;
     }
-    if (!pick_vec(vpt, cs)) return FARN_ERR_UNSUPPORTED;
+    if (!pick_vec(vpt, cs, pb)) return FARN_ERR_UNSUPPORTED;
     pl.variant = cs > 1 ? kVariantCluster : kVariantRow;
     pl.cs = cs; pl.vpt = vpt; pl.threads = (int)threads;
     pl.grid = T * cs;
@@ -321,13 +336,17 @@ const char* farn_status_string(int status) {
   return "unknown status";
 }
 
-int farn_check_args(const void* const* partials, int W, const void* residual,
-                    const void* weight, float eps, int64_t T, int64_t H,
-                    const void* reduced_out, const void* residual_out,
-                    const void* norm_out) {
+}  // extern "C"
+
+namespace {
+
+// The argument checks for partials of `pb` bytes per element.
+int check_args_pb(const void* const* partials, int W, int pb, const void* residual,
+                  const void* weight, float eps, int64_t T, int64_t H,
+                  const void* reduced_out, const void* residual_out, const void* norm_out) {
   if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1) return FARN_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
-  if (H > INT64_MAX / 2 || (T > 0 && T > INT64_MAX / (2 * H))) return FARN_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 4 || (T > 0 && T > INT64_MAX / (4 * H))) return FARN_ERR_INVALID_ARG;
   // With no rows nothing is read or written: empty tensors may have null
   // data pointers.
   if (T == 0) return FARN_OK;
@@ -335,18 +354,34 @@ int farn_check_args(const void* const* partials, int W, const void* residual,
     return FARN_ERR_INVALID_ARG;
   for (int r = 0; r < W; ++r)
     if (!partials[r]) return FARN_ERR_INVALID_ARG;
-  const int64_t nb = T * H * 2, wb = H * 2;
+  const int64_t nb = T * H * 2, xb = T * H * pb, wb = H * 2;
   const void* outs[3] = {reduced_out, residual_out, norm_out};
   for (int i = 0; i < 3; ++i) {
     for (int j = i + 1; j < 3; ++j)
       if (overlaps(outs[i], nb, outs[j], nb)) return FARN_ERR_ALIAS;
     for (int r = 0; r < W; ++r)
-      if (overlaps(outs[i], nb, partials[r], nb)) return FARN_ERR_ALIAS;
+      if (overlaps(outs[i], nb, partials[r], xb)) return FARN_ERR_ALIAS;
     if (overlaps(outs[i], nb, weight, wb)) return FARN_ERR_ALIAS;
     const bool inplace_residual = (i == 1 && residual_out == residual);
     if (!inplace_residual && overlaps(outs[i], nb, residual, nb)) return FARN_ERR_ALIAS;
   }
   return FARN_OK;
+}
+
+int dtype_bytes(int dtype) {
+  return dtype == FARN_BF16 ? 2 : (dtype == FARN_F32 ? 4 : 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+int farn_check_args(const void* const* partials, int W, const void* residual,
+                    const void* weight, float eps, int64_t T, int64_t H,
+                    const void* reduced_out, const void* residual_out,
+                    const void* norm_out) {
+  return check_args_pb(partials, W, 2, residual, weight, eps, T, H, reduced_out, residual_out,
+                       norm_out);
 }
 
 int farn_create(farn_ctx** out, int device) {
@@ -372,12 +407,13 @@ int farn_create(farn_ctx** out, int device) {
   // and must still fit on a GPC, which the occupancy query answers.
   c->max_cluster = 8;
   {
-    VecKernel k16 = pick_vec(1, 16);
+    VecKernel k16 = pick_vec(1, 16, 2);
     if (cudaFuncSetAttribute((const void*)k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       bool ok16 = true;
-      for (int vpt = 1; vpt <= 4; vpt *= 2) {
-        VecKernel k = pick_vec(vpt, 16);
+      for (int i = 0; i < 6 && ok16; ++i) {
+        const int vpt = 1 << (i % 3), pb = i < 3 ? 2 : 4;
+        VecKernel k = pick_vec(vpt, 16, pb);
         if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) { ok16 = false; break; }
         cudaLaunchConfig_t cfg = {};
@@ -428,20 +464,20 @@ int farn_create(farn_ctx** out, int device) {
       return FARN_ERR_CUDA;
     }
   }
-  c->stage_regs4 = c->stage_regs2 = 0;
+  memset(c->stage_regs, 0, sizeof c->stage_regs);
   for (int vpt = 2; vpt <= 4; vpt *= 2) {
-    for (int r = 8; r <= 16; r += 4) {
+    for (int i = 0; i < 3; ++i) {
       // dynamic + static shared memory may not exceed the opt-in limit
       cudaFuncAttributes fa;
-      if (cudaFuncGetAttributes(&fa, (const void*)pick_stage(vpt, r)) != cudaSuccess ||
-          cudaFuncSetAttribute((const void*)pick_stage(vpt, r),
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+      const void* k = (const void*)pick_stage(vpt, kStageDepths[i]);
+      if (cudaFuncGetAttributes(&fa, k) != cudaSuccess ||
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {
         delete c;
         cudaGetLastError();
         return FARN_ERR_CUDA;
       }
-      int& regs = vpt >= 4 ? c->stage_regs4 : c->stage_regs2;
+      int& regs = c->stage_regs[vpt >= 4];
       if (fa.numRegs > regs) regs = fa.numRegs;
     }
   }
@@ -507,15 +543,25 @@ int farn_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, const void* cons
               const void* residual, const void* weight, const void* reduced_out,
               const void* residual_out, const void* norm_out, int* variant,
               int* cluster_size, int* threads) {
+  return farn_plan_typed(ctx, FARN_BF16, W, T, H, partials, residual, weight, reduced_out,
+                         residual_out, norm_out, variant, cluster_size, threads);
+}
+
+int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int W, int64_t T, int64_t H,
+                    const void* const* partials, const void* residual, const void* weight,
+                    const void* reduced_out, const void* residual_out, const void* norm_out,
+                    int* variant, int* cluster_size, int* threads) {
   if (!ctx || !variant || !cluster_size || !threads) return FARN_ERR_INVALID_ARG;
-  int st = farn_check_args(partials, W, residual, weight, 1.0f, T, H, reduced_out,
-                           residual_out, norm_out);
+  const int pb = dtype_bytes(partial_dtype);
+  if (!pb) return FARN_ERR_INVALID_ARG;
+  int st = check_args_pb(partials, W, pb, residual, weight, 1.0f, T, H, reduced_out,
+                         residual_out, norm_out);
   if (st != FARN_OK) return st;
   Plan pl;
   st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out, H),
-                 &pl);
+                 pb, &pl);
   if (st != FARN_OK) return st;
   *variant = pl.variant;
   *cluster_size = pl.cs;
@@ -527,9 +573,19 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
                  const void* residual, const void* weight, float eps, int64_t T,
                  int64_t H, void* reduced_out, void* residual_out, void* norm_out,
                  cudaStream_t stream) {
+  return farn_forward_typed(ctx, partials, FARN_BF16, W, residual, weight, eps, T, H,
+                            reduced_out, residual_out, norm_out, stream);
+}
+
+int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
+                       int W, const void* residual, const void* weight, float eps, int64_t T,
+                       int64_t H, void* reduced_out, void* residual_out, void* norm_out,
+                       cudaStream_t stream) {
   if (!ctx) return FARN_ERR_INVALID_ARG;
-  int st = farn_check_args(partials, W, residual, weight, eps, T, H, reduced_out,
-                           residual_out, norm_out);
+  const int pb = dtype_bytes(partial_dtype);
+  if (!pb) return FARN_ERR_INVALID_ARG;
+  int st = check_args_pb(partials, W, pb, residual, weight, eps, T, H, reduced_out,
+                         residual_out, norm_out);
   if (st != FARN_OK) return st;
   if (T == 0) return FARN_OK;
   if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
@@ -539,7 +595,7 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
   st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out, H),
-                 &pl);
+                 pb, &pl);
   if (st != FARN_OK) return st;
 
   farn::Params prm;
@@ -589,13 +645,13 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
 
   cudaError_t err;
   if (pl.variant == kVariantGeneric) {
-    err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel, prm);
+    err = cudaLaunchKernelEx(&cfg, pick_generic(pb), prm);
   } else if (pl.variant == kVariantBulk) {
     err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm);
   } else if (pl.variant == kVariantStage) {
     err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r), prm);
   } else {
-    VecKernel k = pick_vec(pl.vpt, pl.cs);
+    VecKernel k = pick_vec(pl.vpt, pl.cs, pb);
     err = cudaLaunchKernelEx(&cfg, k, prm);
   }
   if (err != cudaSuccess) {

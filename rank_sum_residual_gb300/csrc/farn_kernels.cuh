@@ -97,6 +97,14 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Eight fp32 partial values (two 16-byte vectors) added in place.
+__device__ __forceinline__ void add8f(float* acc, uint4 a, uint4 b) {
+  acc[0] += __uint_as_float(a.x); acc[1] += __uint_as_float(a.y);
+  acc[2] += __uint_as_float(a.z); acc[3] += __uint_as_float(a.w);
+  acc[4] += __uint_as_float(b.x); acc[5] += __uint_as_float(b.y);
+  acc[6] += __uint_as_float(b.z); acc[7] += __uint_as_float(b.w);
+}
+
 __device__ __forceinline__ void add8(float* acc, uint4 v) {
   acc[0] += bf_lo(v.x); acc[1] += bf_hi(v.x);
   acc[2] += bf_lo(v.y); acc[3] += bf_hi(v.y);
@@ -151,13 +159,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // host guarantees H % 8 == 0, (H/8) % CS == 0, 16-byte aligned pointers and
 // blockDim.x * VPT >= sv.
 //
-// Partials are loaded G ranks at a time (G*VPT = 8 vectors in flight per
-// thread per batch, plus the residual of the first batch) and added in
-// rank order.  At most 512 threads per CTA (128 registers per thread).
-template <int VPT, int CS>
+// Partials are loaded G ranks at a time (G*VPT*PV = 8 16-byte loads in
+// flight per thread per batch, plus the residual) and added in rank order.
+// PB is the partials' element size: 2 (bf16) or 4 (fp32, two 16-byte loads
+// per 8 elements); residual, weight and outputs are bf16 either way.  At
+// most 512 threads per CTA (128 registers per thread).
+template <int VPT, int CS, int PB = 2>
 __global__ void __launch_bounds__(512)
 farn_vec_kernel(const __grid_constant__ Params p) {
-  constexpr int G = (8 / VPT) > 0 ? (8 / VPT) : 1;
+  constexpr int PV = PB / 2;
+  constexpr int G = (8 / (VPT * PV)) > 0 ? (8 / (VPT * PV)) : 1;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
@@ -202,23 +213,29 @@ farn_vec_kernel(const __grid_constant__ Params p) {
 
     // a1: rank sum in fp32, rank order 0..W-1.
     for (int r0 = 0; r0 < p.W; r0 += G) {
-      uint4 xv[G][VPT];
+      uint4 xv[G][VPT][PV];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const int r = r0 + g;
-        const uint4* xp = reinterpret_cast<const uint4*>(p.x[r < p.W ? r : 0]) + base;
+        const uint4* xp = reinterpret_cast<const uint4*>(p.x[r < p.W ? r : 0]) + base * PV;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           const int j = tid + k * blockDim.x;
-          xv[g][k] = make_uint4(0u, 0u, 0u, 0u);
-          if (r < p.W && j < sv) xv[g][k] = ld_stream(xp + j);
+#pragma unroll
+          for (int v = 0; v < PV; ++v) {
+            xv[g][k][v] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < p.W && j < sv) xv[g][k][v] = ld_stream(xp + j * PV + v);
+          }
         }
       }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if (r0 + g < p.W) {
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) add8(acc[k], xv[g][k]);
+          for (int k = 0; k < VPT; ++k) {
+            if (PB == 2) add8(acc[k], xv[g][k][0]);
+            else add8f(acc[k], xv[g][k][0], xv[g][k][PV - 1]);
+          }
         }
       }
     }
@@ -315,6 +332,7 @@ farn_vec_kernel(const __grid_constant__ Params p) {
 // -------------------------------------------------------- generic kernel
 // Any H, any alignment: one CTA per row, scalar bf16 accesses, two passes
 // (the second re-reads the residual_out this same thread wrote).
+template <int PB = 2>
 __global__ void __launch_bounds__(256)
 farn_generic_kernel(const __grid_constant__ Params p) {
   const int tid = threadIdx.x;
@@ -334,8 +352,12 @@ farn_generic_kernel(const __grid_constant__ Params p) {
     float ss = 0.0f;
     for (int64_t h = tid; h < p.H; h += blockDim.x) {
       float acc = -0.0f;
-      for (int r = 0; r < p.W; ++r)
-        acc += __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p.x[r])[off + h] << 16);
+      for (int r = 0; r < p.W; ++r) {
+        if (PB == 2)
+          acc += __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p.x[r])[off + h] << 16);
+        else
+          acc += reinterpret_cast<const float*>(p.x[r])[off + h];
+      }
       const uint16_t rb = to_bf16(acc);
       red_out[off + h] = rb;
       const float s = __uint_as_float((uint32_t)rb << 16) +
@@ -647,7 +669,9 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
 // holding registers, and the prefetch runs on across row boundaries while
 // the CTA reduces a row.  A thread only ever reads the slots it filled
 // itself, so the only waits are cp.async.wait_group (its own copies) and
-// the row reduction's __syncthreads.
+// the row reduction's __syncthreads.  bf16 partials only: with fp32
+// partials the register-staged farn_vec_kernel moves each row's twice
+// larger partials at full bandwidth on its own.
 //
 // Shared memory: R * VPT * blockDim.x * 16 bytes, thread-interleaved so a
 // warp's 16-byte accesses are contiguous.

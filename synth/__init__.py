@@ -8,7 +8,8 @@ operator's arithmetic.
 Recipe (the same on device and host): a SplitMix64 counter stream per
 (seed, stream_id), Box-Muller normals or uniforms evaluated in fp64, an
 optional outlier multiplier, fp64 -> fp32 round-to-nearest, then bf16 by
-truncating the fp32 pattern to its upper 16 bits.  ``gen.cu`` states the
+truncating the fp32 pattern to its upper 16 bits (fp32 partials keep the
+fp32 value).  ``gen.cu`` states the
 constants.  The host twin uses numpy's log/cos, the device CUDA's, so the two
 can differ in a rare last bit; parity never depends on that, because every
 GPU parity test feeds the oracle the bytes the device generated.
@@ -69,18 +70,26 @@ class Problem:
     x: Dist
     residual: Dist = Dist(NORMAL, 0.0, 1.0)
     weight: Dist = Dist(NORMAL, 1.0, 0.1)
+    partial_dtype: str = "bf16"      # or "f32"
+
+    @property
+    def partial_bytes(self) -> int:
+        return 4 if self.partial_dtype == "f32" else 2
 
     def algorithmic_bytes(self) -> int:
-        """(W+1)*T*H*2 read + H*2 weight + 3*T*H*2 written."""
-        return (self.W + 1) * self.T * self.H * 2 + self.H * 2 + 3 * self.T * self.H * 2
+        """W*T*H*pb partials + T*H*2 residual + H*2 weight read, 3*T*H*2
+        written (pb = 2 for bf16 partials, 4 for fp32)."""
+        return (self.W * self.T * self.H * self.partial_bytes + self.T * self.H * 2
+                + self.H * 2 + 3 * self.T * self.H * 2)
 
     def with_seed(self, seed: int) -> "Problem":
         return Problem(self.name, self.W, self.T, self.H, self.eps, seed,
-                       self.x, self.residual, self.weight)
+                       self.x, self.residual, self.weight, self.partial_dtype)
 
     def with_T(self, T: int) -> "Problem":
         return Problem(f"{self.name.split('@')[0]}@T{T}", self.W, T, self.H,
-                       self.eps, self.seed, self.x, self.residual, self.weight)
+                       self.eps, self.seed, self.x, self.residual, self.weight,
+                       self.partial_dtype)
 
 
 N01 = Dist(NORMAL, 0.0, 1.0)
@@ -101,6 +110,10 @@ WORKLOADS = {
     "wide": [Problem("wide", 16, 4096, 7168, 1e-6, 0, Dist(NORMAL, 0.0, 1.0 / 16))],
     # residual add + RMSNorm alone (one partial: no rank sum), prefill-sized
     "rmsnorm": [Problem("rmsnorm", 1, 8192, 8192, 1e-6, 0, N01)],
+    # the prefill shape with fp32 partials (e.g. straight from GEMM epilogues)
+    "prefill_f32": [Problem("prefill_f32", 8, 8192, 8192, 1e-6, 0,
+                            Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
+                            N01, Dist(UNIFORM, 0.5, 1.5), "f32")],
 }
 
 
@@ -149,10 +162,32 @@ def host_bf16(n: int, seed: int, stream_id: int, dist: Dist) -> np.ndarray:
     return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
+def host_f32(n: int, seed: int, stream_id: int, dist: Dist) -> np.ndarray:
+    """The recipe kept in fp32 (fp32 partials)."""
+    with np.errstate(over="ignore"):
+        base = _base(seed, stream_id)
+        j = np.arange(n, dtype=np.uint64) * np.uint64(3)
+        u1 = _unit(_mix64(base + (j + np.uint64(1)) * GAMMA))
+        u2 = _unit(_mix64(base + (j + np.uint64(2)) * GAMMA))
+        if dist.kind == NORMAL:
+            v = dist.p0 + np.sqrt(dist.p1) * (np.sqrt(-2.0 * np.log(u1))
+                                              * np.cos(2.0 * np.pi * u2))
+        else:
+            v = dist.p0 + (dist.p1 - dist.p0) * u1
+        if dist.outlier_p > 0:
+            u3 = _unit(_mix64(base + (j + np.uint64(3)) * GAMMA))
+            v = np.where(u3 < dist.outlier_p, v * dist.outlier_scale, v)
+    return v.astype(np.float32)
+
+
 def host_inputs(p: Problem):
-    """(partials list of [T,H], residual [T,H], weight [H]) as uint16 arrays."""
+    """(partials list of [T,H], residual [T,H], weight [H]); partials are
+    uint16 bf16 patterns or float32, residual and weight uint16."""
     n = p.T * p.H
-    xs = [host_bf16(n, p.seed, r, p.x).reshape(p.T, p.H) for r in range(p.W)]
+    if p.partial_dtype == "f32":
+        xs = [host_f32(n, p.seed, r, p.x).reshape(p.T, p.H) for r in range(p.W)]
+    else:
+        xs = [host_bf16(n, p.seed, r, p.x).reshape(p.T, p.H) for r in range(p.W)]
     res = host_bf16(n, p.seed, STREAM_RESIDUAL, p.residual).reshape(p.T, p.H)
     w = host_bf16(p.H, p.seed, STREAM_WEIGHT, p.weight)
     return xs, res, w
@@ -184,6 +219,8 @@ def _load():
             ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double,
             ctypes.c_double, ctypes.c_void_p]
         lib.farn_synth_fill_bf16.restype = ctypes.c_int
+        lib.farn_synth_fill_f32.argtypes = lib.farn_synth_fill_bf16.argtypes
+        lib.farn_synth_fill_f32.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -191,12 +228,14 @@ def _load():
 def fill_device(t, seed: int, stream_id: int, dist: Dist, stream=None) -> None:
     """Fill a contiguous torch bf16 CUDA tensor in place with the recipe."""
     import torch
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise TypeError("fill_device wants a contiguous bf16 CUDA tensor")
+    if t.dtype not in (torch.bfloat16, torch.float32) or not t.is_cuda \
+            or not t.is_contiguous():
+        raise TypeError("fill_device wants a contiguous bf16 or fp32 CUDA tensor")
     s = stream if stream is not None else torch.cuda.current_stream(t.device)
-    rc = _load().farn_synth_fill_bf16(
-        t.data_ptr(), t.numel(), seed, stream_id, dist.kind, dist.p0, dist.p1,
-        dist.outlier_p, dist.outlier_scale, s.cuda_stream)
+    fn = _load().farn_synth_fill_bf16 if t.dtype == torch.bfloat16 \
+        else _load().farn_synth_fill_f32
+    rc = fn(t.data_ptr(), t.numel(), seed, stream_id, dist.kind, dist.p0, dist.p1,
+            dist.outlier_p, dist.outlier_scale, s.cuda_stream)
     if rc != 0:
         raise RuntimeError(f"farn_synth_fill_bf16 failed (rc={rc})")
 
@@ -206,8 +245,9 @@ def device_inputs(p: Problem, device="cuda", seed: int | None = None):
     import torch
     sd = p.seed if seed is None else seed
     xs = []
+    xdt = torch.float32 if p.partial_dtype == "f32" else torch.bfloat16
     for r in range(p.W):
-        t = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=device)
+        t = torch.empty((p.T, p.H), dtype=xdt, device=device)
         fill_device(t, sd, r, p.x)
         xs.append(t)
     res = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=device)

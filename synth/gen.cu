@@ -40,28 +40,41 @@ __device__ inline double unit(uint64_t z) {
   return ((double)(z >> 11) + 0.5) * 0x1.0p-53;
 }
 
+// One value of the recipe, element i of the stream with key `base`.
+__device__ inline float draw(int64_t i, uint64_t base, int dist, double p0, double p1,
+                             double outlier_p, double outlier_scale) {
+  const double kTwoPi = 6.283185307179586476925286766559;
+  uint64_t j = 3ull * (uint64_t)i;
+  double u1 = unit(mix64(base + (j + 1) * kGamma));
+  double u2 = unit(mix64(base + (j + 2) * kGamma));
+  double v;
+  if (dist == 0) {
+    double z = sqrt(-2.0 * log(u1)) * cos(kTwoPi * u2);
+    v = p0 + sqrt(p1) * z;
+  } else {
+    v = p0 + (p1 - p0) * u1;
+  }
+  if (outlier_p > 0.0) {
+    double u3 = unit(mix64(base + (j + 3) * kGamma));
+    if (u3 < outlier_p) v *= outlier_scale;
+  }
+  return (float)v;
+}
+
+__global__ void fill_f32_kernel(float* __restrict__ dst, int64_t n, uint64_t base, int dist,
+                                double p0, double p1, double outlier_p,
+                                double outlier_scale) {
+  int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    dst[i] = draw(i, base, dist, p0, p1, outlier_p, outlier_scale);
+}
+
 __global__ void fill_bf16_kernel(uint16_t* __restrict__ dst, int64_t n,
                                  uint64_t base, int dist, double p0, double p1,
                                  double outlier_p, double outlier_scale) {
-  const double kTwoPi = 6.283185307179586476925286766559;
   int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += stride) {
-    uint64_t j = 3ull * (uint64_t)i;
-    double u1 = unit(mix64(base + (j + 1) * kGamma));
-    double u2 = unit(mix64(base + (j + 2) * kGamma));
-    double v;
-    if (dist == 0) {
-      double z = sqrt(-2.0 * log(u1)) * cos(kTwoPi * u2);
-      v = p0 + sqrt(p1) * z;
-    } else {
-      v = p0 + (p1 - p0) * u1;
-    }
-    if (outlier_p > 0.0) {
-      double u3 = unit(mix64(base + (j + 3) * kGamma));
-      if (u3 < outlier_p) v *= outlier_scale;
-    }
-    float f = (float)v;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float f = draw(i, base, dist, p0, p1, outlier_p, outlier_scale);
     dst[i] = (uint16_t)(__float_as_uint(f) >> 16);
   }
 }
@@ -87,6 +100,23 @@ int farn_synth_fill_bf16(void* dst, int64_t n, uint64_t seed,
   int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
   fill_bf16_kernel<<<blocks, threads, 0, stream>>>(
       (uint16_t*)dst, n, base, dist, p0, p1, outlier_p, outlier_scale);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+// The same recipe kept in fp32 (no bf16 truncation): dst is float[n].
+int farn_synth_fill_f32(void* dst, int64_t n, uint64_t seed, uint64_t stream_id, int dist,
+                        double p0, double p1, double outlier_p, double outlier_scale,
+                        cudaStream_t stream) {
+  if (n < 0 || (n > 0 && dst == nullptr) || (dist != 0 && dist != 1) ||
+      (dist == 0 && !(p1 >= 0.0)) || !(outlier_p >= 0.0))
+    return -1;
+  if (n == 0) return 0;
+  uint64_t base = mix64(seed ^ mix64(stream_id + kGamma));
+  int threads = 256;
+  int64_t want = (n + threads - 1) / threads;
+  int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
+  fill_f32_kernel<<<blocks, threads, 0, stream>>>((float*)dst, n, base, dist, p0, p1,
+                                                  outlier_p, outlier_scale);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

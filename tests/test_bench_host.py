@@ -78,7 +78,7 @@ def test_reference_arm_json_line(monkeypatch):
 @pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
 def test_algorithmic_bytes_formula(name):
     for p in synth.workload(name):
-        read = (p.W + 1) * p.T * p.H * 2 + p.H * 2
+        read = p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
         write = 3 * p.T * p.H * 2
         assert p.algorithmic_bytes() == read + write
         assert bench.call_bytes(p, p.T) == read + write

@@ -57,11 +57,18 @@ def make_ctx(**env):
                 os.environ[k] = v
 
 
+def host(t):
+    """Partials for the oracle: bf16 patterns, or fp32 values as they are."""
+    if t.dtype == torch.float32:
+        return t.detach().cpu().numpy()
+    return u16(t)
+
+
 def oracle_rows(O, xs, res, w, eps, rows=None):
     if rows is None:
-        return O.forward([u16(x) for x in xs], u16(res), u16(w), eps)
+        return O.forward([host(x) for x in xs], u16(res), u16(w), eps)
     idx = torch.as_tensor(rows, device=res.device)
-    return O.forward([u16(x.index_select(0, idx)) for x in xs],
+    return O.forward([host(x.index_select(0, idx)) for x in xs],
                      u16(res.index_select(0, idx)), u16(w), eps)
 
 
@@ -402,7 +409,7 @@ def test_bad_eps_and_shapes_raise(dev):
     with pytest.raises(ValueError):
         farn.forward(xs, res[:, :32].contiguous(), w, 1e-6)
     with pytest.raises(TypeError):
-        farn.forward([x.float() for x in xs], res, w, 1e-6)
+        farn.forward([x.half() for x in xs], res, w, 1e-6)
 
 
 def test_injected_launch_fault_launches_nothing(dev):
@@ -499,3 +506,114 @@ def test_full_size_in_place(O, dev, name):
     assert_parity(got, want, f"{name} in place")
     del xs, res, w, red, nrm
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------- fp32 partials
+def _f32(name, T, W=None, H=None):
+    p = synth.workload(name)[0].with_T(T) if name in synth.WORKLOADS else None
+    if p is None or W is not None:
+        p = synth.Problem(name, W, T, H, 1e-6, 31, synth.N01)
+    return synth.Problem(p.name, p.W, p.T, p.H, p.eps, p.seed, p.x, p.residual,
+                         p.weight, "f32")
+
+
+@pytest.mark.parametrize("prob", [
+    ("prefill_f32", 333), ("prefill_f32", 2500), ("nonpow2", 517), ("wide", 300),
+    ("wide", 2100), ("dec", 1, 8, 4096), ("dec", 5, 8, 4096), ("dec", 64, 8, 4096),
+    ("odd", 3, 3, 1000), ("w1", 40, 1, 2048), ("w32", 6, 32, 1024)],
+    ids=lambda p: "-".join(str(v) for v in p))
+def test_f32_partials(O, dev, prob):
+    """fp32 partials (residual, weight, outputs bf16) against the oracle's
+    fp32-partial path, on the default launch plan."""
+    p = _f32(*prob) if len(prob) == 2 else _f32(prob[0], prob[1], prob[2], prob[3])
+    run_and_check(O, p, dev, what=f"f32 partials {prob}")
+
+
+def test_f32_partials_full_size_sampled(O, dev):
+    p = synth.workload("prefill_f32")[0]
+    run_and_check(O, p, dev, rows=sample_rows(p.T, 128, seed=2))
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("env", [
+    dict(FARN_VARIANT="row"), dict(FARN_VARIANT="generic"),
+    dict(FARN_VARIANT="cluster", FARN_CLUSTER=2), dict(FARN_VARIANT="cluster", FARN_CLUSTER=8),
+    dict(FARN_VARIANT="cluster", FARN_CLUSTER=16), dict(FARN_VARIANT="row", FARN_VPT=4),
+    dict(FARN_VARIANT="row", FARN_VPT=1), dict(FARN_VARIANT="row", FARN_VPT=2)],
+    ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
+def test_f32_partials_forced_variants(O, dev, env):
+    p = _f32("v", 37, 6, 4096)
+    ctx = make_ctx(**env)
+    try:
+        run_and_check(O, p, dev, ctx=ctx, what=f"f32 {env}")
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("variant", ["bulk", "stage"])
+def test_f32_partials_staged_kernels_refused(dev, variant):
+    """The TMA- and cp.async-staged kernels stage bf16 rows only: forcing
+    either with fp32 partials is refused (the row kernel serves them)."""
+    p = _f32("v", 4, 2, 2048)
+    xs, res, w = synth.device_inputs(p, dev)
+    ctx = make_ctx(FARN_VARIANT=variant)
+    try:
+        with pytest.raises(farn.FarnError) as e:
+            farn.forward(xs, res, w, p.eps, ctx=ctx)
+        assert e.value.status == farn.FARN_ERR_UNSUPPORTED
+    finally:
+        ctx.close()
+
+
+def test_f32_partials_misaligned_and_specials(O, dev):
+    W, T, H = 3, 5, 1024
+    p = _f32("m", T, W, H)
+    xs0, res, w = synth.device_inputs(p, dev)
+    xs = []
+    for x in xs0:                        # 4-byte offset: not 16-byte aligned
+        buf = torch.empty(x.numel() + 1, dtype=torch.float32, device=dev)
+        v = buf[1:].view(T, H)
+        v.copy_(x)
+        xs.append(v)
+    xs[0][0, 3] = float("nan")
+    xs[1][1, 7] = float("inf")
+    xs[2][2, 9] = 3.0e38
+    xs[1][2, 9] = 3.0e38                 # overflows the fp32 sum
+    xs[0][3].zero_(); xs[1][3].zero_(); xs[2][3].zero_()
+    xs[0][4, 0] = 1.0
+    xs[1][4, 0] = 2.0 ** -10
+    xs[2][4, 0] = -1.0                   # (1 + 2^-10) - 1 = 2^-10 exactly
+    assert xs[0].data_ptr() % 16 == 4
+    out = farn.forward(xs, res, w, p.eps)
+    torch.cuda.synchronize()
+    got = [u16(t) for t in out]
+    assert_parity(got, oracle_rows(O, xs, res, w, p.eps), "f32 misaligned + specials")
+    assert got[0][4, 0] == 0x3A80
+
+
+def test_f32_partials_alias_uses_four_byte_extent(dev):
+    """An output over the second half of an fp32 partial overlaps it (the
+    partial spans T*H*4 bytes), so it is refused."""
+    T, H = 8, 256
+    x = torch.zeros((T, H), dtype=torch.float32, device=dev)
+    res = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+    w = torch.ones(H, dtype=torch.bfloat16, device=dev)
+    inside = x.view(torch.bfloat16).view(-1)[T * H: 2 * T * H].view(T, H)
+    outs = (inside, torch.empty_like(res), torch.empty_like(res))
+    with pytest.raises(farn.FarnError) as e:
+        farn.forward([x], res, w, 1e-6, out=outs)
+    assert e.value.status == farn.FARN_ERR_ALIAS
+
+
+def test_f32_partials_plan(dev):
+    c = farn.Context(0)
+    try:
+        a, g = (1 << 40), (1 << 34)
+        args = ([a] * 8, a + g, a + 2 * g, a + 3 * g, a + 4 * g, a + 5 * g)
+        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 8192, 8192, *args)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 8192, *args)[0] == "stage"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 2, 4096, *args)[0] == "cluster"
+        with pytest.raises(farn.FarnError):
+            farn.farn_plan_typed(c.handle, 7, 8, 2, 4096, *args)
+    finally:
+        c.close()
