@@ -617,3 +617,58 @@ def test_f32_partials_plan(dev):
             farn.farn_plan_typed(c.handle, 7, 8, 2, 4096, *args)
     finally:
         c.close()
+
+
+# --------------------------------------------------- graphs and streams
+@pytest.mark.parametrize("name,T", [("decode", 1), ("decode", 64), ("prefill", 2300),
+                                    ("wide", 300), ("prefill_f32", 40)])
+def test_cuda_graph_capture_and_replay(O, dev, name, T):
+    """Calls captured in a CUDA graph (as the benchmark runs them, with
+    programmatic dependent launch) give the oracle's results on replay,
+    including after the inputs change in place between replays."""
+    p = synth.workload(name)[0].with_T(T)
+    xs, res, w = synth.device_inputs(p, dev)
+    outs = tuple(torch.empty_like(res) for _ in range(3))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        farn.forward(xs, res, w, p.eps, out=outs)          # warm-up / module load
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        farn.forward(xs, res, w, p.eps, out=outs, stream=s)
+        farn.forward(xs, res, w, p.eps, out=outs, stream=s)  # two dependent launches
+    for k in range(2):
+        if k:
+            synth.fill_device(xs[0], 99, 0, p.x)            # new values, same buffers
+            torch.cuda.synchronize()
+        for o in outs:
+            o.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_parity([u16(t) for t in outs], oracle_rows(O, xs, res, w, p.eps),
+                      f"graph replay {k} {name} T={T}")
+
+
+def test_two_streams_concurrently(O, dev):
+    """Independent calls on two streams at once (one long, one decode-sized)."""
+    pa = synth.workload("prefill")[0].with_T(4096)
+    pb = synth.workload("decode")[-1]
+    a = synth.device_inputs(pa, dev)
+    b = synth.device_inputs(pb, dev)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs_a, outs_b = [], []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            outs_a.append(farn.forward(*a, pa.eps))
+        with torch.cuda.stream(s2):
+            outs_b.append(farn.forward(*b, pb.eps))
+    torch.cuda.synchronize()
+    rows = sample_rows(pa.T, 64, seed=4)
+    idx = torch.as_tensor(rows, device=dev)
+    want_a = oracle_rows(O, *a, pa.eps, rows)
+    want_b = oracle_rows(O, *b, pb.eps)
+    for oa, ob in zip(outs_a, outs_b):
+        assert_parity([u16(t.index_select(0, idx)) for t in oa], want_a, "stream 1")
+        assert_parity([u16(t) for t in ob], want_b, "stream 2")
