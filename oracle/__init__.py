@@ -75,6 +75,13 @@ def _declare(lib):
                                        u16p, ctypes.c_float, ctypes.c_int64,
                                        ctypes.c_int64, u16p, u16p, u16p]
     lib.oracle_forward_f32.restype = ctypes.c_int
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_e4m3_sat.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
+    lib.oracle_quant_e4m3_row.argtypes = [u16p, ctypes.c_int64, u8p]
+    lib.oracle_quant_e4m3_row.restype = ctypes.c_float
     return lib
 
 
@@ -178,6 +185,35 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_forward rejected its arguments (rc={rc})")
         return reduced, ro, norm
+
+
+def _Oracle_quant(self, norm):
+    """E4M3 quantisation of bf16 norm_out rows [T,H]: (q uint8 [T,H],
+    scale float32 [T])."""
+    norm = _u16(norm)
+    if norm.ndim == 1:
+        norm = norm[None, :]
+    T, H = norm.shape
+    q = np.empty((T, H), np.uint8)
+    scale = np.empty(T, np.float32)
+    for t in range(T):
+        row = np.ascontiguousarray(norm[t])
+        scale[t] = self.lib.oracle_quant_e4m3_row(
+            _p(row), H, q[t].ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)))
+    return q, scale
+
+
+def _Oracle_e4m3(self, f: float) -> int:
+    return int(self.lib.oracle_f32_to_e4m3_sat(float(np.float32(f))))
+
+
+def _Oracle_e4m3_to_f32(self, b: int) -> float:
+    return float(self.lib.oracle_e4m3_to_f32(int(b)))
+
+
+Oracle.quant_e4m3 = _Oracle_quant
+Oracle.f32_to_e4m3 = _Oracle_e4m3
+Oracle.e4m3_to_f32 = _Oracle_e4m3_to_f32
 
 
 def forward(xs, residual, weight, eps: float):

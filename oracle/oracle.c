@@ -204,3 +204,74 @@ int oracle_forward_f32(const float *const *x, int W, const uint16_t *residual,
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------
+ * Fused FP8 quantisation of norm_out (an extension the page does not
+ * describe: the next layer's GEMM input in the OCP 8-bit E4M3 format).
+ *
+ * E4M3 ("FN" flavour): 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits; no infinities; S.1111.111 is NaN; the largest finite magnitude is
+ * 448 = 1.75 * 2^8; subnormals are multiples of 2^-9.
+ *
+ * Reading: per row t, amax = the largest |norm_out[t,h]| (NaN ignored, as
+ * IEEE maxNum does), scale[t] = amax / 448 (fp32 division; 1 if amax is 0),
+ * q[t,h] = E4M3(norm_out[t,h] / scale[t]) with round to nearest even and
+ * saturation of any magnitude above 448 (infinity included) to 448; NaN
+ * stays NaN.  Given the bf16 norm_out row, scale and q are unique.
+ * ------------------------------------------------------------------- */
+float oracle_e4m3_to_f32(uint8_t b)
+{
+    float sign = (b & 0x80u) ? -1.0f : 1.0f;
+    int e = (b >> 3) & 0xF, m = b & 0x7;
+    if (e == 0xF && m == 0x7)
+        return NAN;
+    if (e == 0)
+        return sign * ldexpf((float)m, -9);
+    return sign * ldexpf(1.0f + (float)m / 8.0f, e - 7);
+}
+
+uint8_t oracle_f32_to_e4m3_sat(float f)
+{
+    if (isnan(f))
+        return 0x7Fu;
+    uint8_t sign = signbit(f) ? 0x80u : 0x00u;
+    float a = fabsf(f);
+    if (a > 448.0f)
+        return (uint8_t)(sign | 0x7Eu);          /* saturate to 448 */
+    if (a == 0.0f)
+        return sign;
+    int e2;
+    frexpf(a, &e2);                 /* a = m * 2^e2, m in [0.5, 1) */
+    int E = e2 - 1;                 /* 2^E <= a < 2^(E+1) */
+    if (E < -6)
+        E = -6;                     /* subnormal range: step 2^-9 */
+    float step = ldexpf(1.0f, E - 3);
+    float k = rintf(a / step);      /* exact division; rint: nearest even */
+    float v = k * step;
+    if (v > 448.0f)
+        v = 448.0f;
+    if (v == 0.0f)
+        return sign;
+    if (v < ldexpf(1.0f, -6))       /* subnormal: v = k * 2^-9, k in 1..7 */
+        return (uint8_t)(sign | (uint8_t)(v / ldexpf(1.0f, -9)));
+    frexpf(v, &e2);
+    E = e2 - 1;
+    int mant = (int)((v / ldexpf(1.0f, E) - 1.0f) * 8.0f);
+    return (uint8_t)(sign | (uint8_t)((E + 7) << 3) | (uint8_t)mant);
+}
+
+/* One row: returns the scale, writes q[0..H). */
+float oracle_quant_e4m3_row(const uint16_t *norm, int64_t H, uint8_t *q)
+{
+    float amax = 0.0f;
+    for (int64_t h = 0; h < H; ++h) {
+        float v = fabsf(oracle_bf16_to_f32(norm[h]));
+        if (v > amax)               /* NaN never compares greater */
+            amax = v;
+    }
+    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int64_t h = 0; h < H; ++h)
+        q[h] = oracle_f32_to_e4m3_sat(oracle_bf16_to_f32(norm[h]) / scale);
+    return scale;
+}
+

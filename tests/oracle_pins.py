@@ -357,4 +357,149 @@ def pin_f32_partials_equal_bf16_path_on_bf16_values(O):
         assert np.array_equal(u, v)
 
 
+# ------------------------------------------------------- E4M3 quantisation
+E4M3_MAX = Fraction(448)
+
+
+def e4m3_exact(q) -> int:
+    """Exact rational (or float special) -> E4M3 pattern, nearest even,
+    magnitudes above 448 (and infinities) saturated, from the format
+    definition (1 sign, 4 exponent bits bias 7, 3 fraction bits, S.1111.111
+    NaN, subnormal step 2^-9)."""
+    if isinstance(q, float):
+        if np.isnan(q):
+            return 0x7F
+        if np.isinf(q):
+            return 0xFE if q < 0 else 0x7E
+        if q == 0.0:
+            return 0x80 if np.signbit(q) else 0x00
+        q = Fraction(q)
+    sign = 0x80 if q < 0 else 0
+    a = abs(q)
+    if a > E4M3_MAX:
+        return sign | 0x7E
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -6)
+    step = Fraction(2) ** (e - 3)
+    n = a / step
+    k = n.numerator // n.denominator
+    rem = n - k
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and k % 2 == 1):
+        k += 1
+    v = k * step
+    if v > E4M3_MAX:
+        v = E4M3_MAX
+    if v == 0:
+        return sign
+    if v < Fraction(2) ** -6:
+        return sign | int(v / Fraction(2) ** -9)
+    e = v.numerator.bit_length() - v.denominator.bit_length()
+    if Fraction(2) ** e > v:
+        e -= 1
+    mant = (v / Fraction(2) ** e - 1) * 8
+    assert mant.denominator == 1
+    return sign | ((e + 7) << 3) | int(mant)
+
+
+def pin_e4m3_decode_all_patterns(O):
+    for b in range(256):
+        got = O.e4m3_to_f32(b)
+        e, m = (b >> 3) & 0xF, b & 7
+        if e == 0xF and m == 7:
+            assert np.isnan(got)
+            continue
+        want = (Fraction(m, 512) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7))
+        want = -want if b & 0x80 else want
+        assert Fraction(got) == want, hex(b)
+    assert O.e4m3_to_f32(0x7E) == 448.0 and O.e4m3_to_f32(0x01) == 2.0 ** -9
+
+
+def pin_e4m3_rounding_vs_exact(O):
+    rng = np.random.default_rng(29)
+    vals = list((rng.normal(size=3000) * np.exp2(rng.integers(-14, 11, 3000))).astype(np.float32))
+    # ties and neighbours at every binade, subnormal ties, saturation edges
+    for e in range(-9, 9):
+        for m in range(8):
+            base = (1 + m / 8) * 2.0 ** e if e >= -6 else m * 2.0 ** -9
+            step = 2.0 ** (max(e, -6) - 3)
+            vals += [np.float32(base + step / 2), np.float32(base + step / 2) * np.float32(1 + 2 ** -20),
+                     np.float32(base + step / 2) * np.float32(1 - 2 ** -20)]
+    vals += [np.float32(v) for v in (448, 455.9, 464, 464.1, 1e30, -1e30, 2.0 ** -10,
+                                      3 * 2.0 ** -10, 0.0, -0.0, float("inf"), float("-inf"))]
+    for v in vals:
+        got = O.f32_to_e4m3(float(v))
+        want = e4m3_exact(float(v) if (v == 0 or not np.isfinite(v)) else Fraction(float(v)))
+        assert got == want, (float(v), hex(got), hex(want))
+    assert O.f32_to_e4m3(float("nan")) & 0x7F == 0x7F
+
+
+def pin_e4m3_matches_torch_cast(O):
+    """The library routine: torch's float8_e4m3fn cast (round to nearest
+    even) agrees on finite values within range."""
+    torch = __import__("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        return
+    rng = np.random.default_rng(31)
+    v = np.clip((rng.normal(size=4000) * np.exp2(rng.integers(-12, 9, 4000))), -448, 448)
+    v = v.astype(np.float32)
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([O.f32_to_e4m3(float(x)) for x in v], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def pin_quant_row_closed_forms(O):
+    one = bx.bits(1)
+    # [1, -2, 0.5, 0]: amax 2, scale 2/448, values map to 224, -448, 112, 0
+    row = np.array([bx.bits(1), bx.bits(-2), bx.bits(0.5), 0], np.uint16)
+    q, sc = O.quant_e4m3(row)
+    assert abs(sc[0] - np.float32(2) / np.float32(448)) == 0
+    assert [O.e4m3_to_f32(int(b)) for b in q[0]] == [224.0, -448.0, 112.0, 0.0]
+    # all-zero row: scale 1, q zero
+    q, sc = O.quant_e4m3(np.zeros(8, np.uint16))
+    assert sc[0] == 1.0 and not q.any()
+    # a NaN element is ignored by amax and quantises to NaN
+    row = np.array([bx.QNAN, bx.bits(4), bx.bits(-1)], np.uint16)
+    q, sc = O.quant_e4m3(row)
+    assert sc[0] == np.float32(4) / np.float32(448) and (q[0][0] & 0x7F) == 0x7F
+    assert O.e4m3_to_f32(int(q[0][1])) == 448.0
+    # the amax element always lands on +-448
+    rng = np.random.default_rng(37)
+    rows = (rng.normal(size=(20, 64)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    q, sc = O.quant_e4m3(rows)
+    for t in range(20):
+        vals = bx.to_f64(rows[t])
+        i = int(np.argmax(np.abs(vals)))
+        assert abs(O.e4m3_to_f32(int(q[t][i]))) == 448.0
+    del one
+
+
+def pin_quant_row_power_of_two_invariance(O):
+    """Scaling a row by 2^k scales its scale by 2^k and leaves q unchanged."""
+    rng = np.random.default_rng(41)
+    x = rng.normal(size=(6, 96)).astype(np.float32)
+    base = (x.view(np.uint32) >> 16).astype(np.uint16)
+    q0, s0 = O.quant_e4m3(base)
+    for k in (-3, 1, 5):
+        xs = ((x * np.float32(2.0 ** k)).view(np.uint32) >> 16).astype(np.uint16)
+        q1, s1 = O.quant_e4m3(xs)
+        assert np.array_equal(q0, q1) and np.array_equal(s1, s0 * np.float32(2.0 ** k))
+
+
+def pin_quant_row_vs_exact_division(O):
+    """q = E4M3(x / scale) with the division rounded to fp32 first."""
+    rng = np.random.default_rng(43)
+    rows = (rng.normal(size=(8, 48)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    q, sc = O.quant_e4m3(rows)
+    for t in range(8):
+        vals = bx.to_f64(rows[t])
+        amax = np.float32(np.abs(vals).max())
+        scale = np.float32(amax / np.float32(448))
+        assert sc[t] == scale
+        for h in range(48):
+            d = np.float32(np.float32(vals[h]) / scale)
+            assert int(q[t][h]) == e4m3_exact(Fraction(float(d)) if d != 0 else float(d))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
