@@ -58,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm",
-                             "prefill_f32"])
+                             "prefill_f32", "prefill_fp8"])
     ap.add_argument("--in-place", action="store_true",
                     help="write residual_out over the residual (in-place residual update)")
     ap.add_argument("--impl", default="farn", choices=["farn", "reference"])
@@ -196,9 +196,8 @@ def gpu_id_for(dev_index):
 
 # -------------------------------------------------------- CPU (the oracle)
 def row_bytes(p) -> int:
-    """Algorithmic bytes of one row of a call (weight counted per call):
-    W partial rows of H elements, the residual row, three output rows."""
-    return p.W * p.H * p.partial_bytes + 4 * p.H * 2
+    """Algorithmic bytes of one row of a call (weight counted per call)."""
+    return (p.algorithmic_bytes() - p.H * 2) // p.T
 
 
 def call_bytes(p, rows) -> int:
@@ -226,7 +225,9 @@ def time_oracle_rows(sample, rows_total_target=None, seconds=10.0):
     t0 = time.perf_counter()
     while True:
         for p, xs, res, w in sample:
-            O.forward(xs, res, w, p.eps)
+            outs = O.forward(xs, res, w, p.eps)
+            if p.fp8_out:
+                O.quant_e4m3(outs[2])
             r = res.shape[0]
             nbytes += call_bytes(p, r)
             nrows += r
@@ -270,7 +271,9 @@ def run_reference(args):
         for _ in range(rows_per_step):
             p, xs, res, w, t = flat[cursor % len(flat)]
             cursor += 1
-            O.forward([x[t:t + 1] for x in xs], res[t:t + 1], w, p.eps)
+            outs = O.forward([x[t:t + 1] for x in xs], res[t:t + 1], w, p.eps)
+            if p.fp8_out:
+                O.quant_e4m3(outs[2])
             b += call_bytes(p, 1)
             n += 1
         return b, n
@@ -355,20 +358,19 @@ def run_gpu(args):
             calls = []
             for p in problems:
                 xs, res, w = synth.device_inputs(p, dev, seed=p.seed + 7919 * k)
-                outs = tuple(torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev)
-                             for _ in range(3))
+                outs = make_outputs(p, dev)
                 if args.in_place:
                     # residual_out is the residual buffer itself; every step
                     # then reads the residual the previous step over that
                     # copy wrote, which leaves the bytes moved unchanged
-                    outs = (outs[0], res, outs[2])
+                    outs = (outs[0], res) + tuple(outs[2:])
                 calls.append((p, xs, res, w, outs))
             sets.append(calls)
     stream.synchronize()
 
     def launch(call):
         p, xs, res, w, outs = call
-        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
+        call_forward(p, xs, res, w, outs, ctx, stream)
 
     def step(k):
         for call in sets[k]:
@@ -565,7 +567,38 @@ def plan_args(call):
     p, xs, res, w, outs = call
     return (farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16, p.W, p.T, p.H,
             [x.data_ptr() for x in xs], res.data_ptr(), w.data_ptr(),
-            outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr())
+            outs[0].data_ptr(), outs[1].data_ptr(),
+            outs[2].data_ptr() if outs[2] is not None else 0,
+            farn.FARN_PLAN_FP8_OUT if p.fp8_out else 0)
+
+
+def make_outputs(p, dev):
+    """(reduced, residual_out, norm_out or None[, E4M3 bytes, row scales])."""
+    import torch
+    outs = [torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    outs.append(torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev)
+                if p.norm_out else None)
+    if p.fp8_out:
+        outs.append(torch.empty((p.T, p.H), dtype=torch.uint8, device=dev))
+        outs.append(torch.empty((p.T,), dtype=torch.float32, device=dev))
+    return tuple(outs)
+
+
+def call_forward(p, xs, res, w, outs, ctx, stream):
+    """One operator call through the binding of the C ABI."""
+    import rank_sum_residual_gb300 as farn
+    if not p.fp8_out:
+        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
+        return
+    s = stream if stream is not None else __import__("torch").cuda.current_stream()
+    st = farn.farn_forward_quant(
+        (ctx or farn._context_for(res.device.index)).handle, [x.data_ptr() for x in xs],
+        farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16, len(xs), res.data_ptr(),
+        w.data_ptr(), p.eps, p.T, p.H, outs[0].data_ptr(), outs[1].data_ptr(),
+        outs[2].data_ptr() if outs[2] is not None else 0, outs[3].data_ptr(),
+        outs[4].data_ptr(), s.cuda_stream)
+    if st != farn.FARN_OK:
+        raise farn.FarnError(st, "farn_forward_quant")
 
 
 def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
@@ -587,15 +620,13 @@ def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
             synth.fill_device(x, p.seed + 1, r, p.x)
         synth.fill_device(res, p.seed + 1, synth.STREAM_RESIDUAL, p.residual)
         synth.fill_device(w, p.seed + 1, synth.STREAM_WEIGHT, p.weight)
-        outs = [torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
-                for _ in range(3)]
+        outs = [make_outputs(p, dev) for _ in range(copies)]
         reps = max(min_launches, copies)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(reps):
                 c = i % copies
-                farn.forward([x[c] for x in xs], res[c], w, p.eps,
-                             out=tuple(o[c] for o in outs), ctx=ctx)
+                call_forward(p, [x[c] for x in xs], res[c], w, outs[c], ctx, None)
         g.replay()
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -624,12 +655,12 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     import torch
     import rank_sum_residual_gb300 as farn
 
-    # inputs packed as bytes (partials may be fp32), outputs bf16
+    # inputs and outputs packed as bytes (fp32 partials, E4M3 outputs)
     in_bytes = sum(p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
                    for p in problems)
-    out_elems = sum(3 * p.T * p.H for p in problems)
+    out_bytes = sum(p.write_bytes() for p in problems)
     host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    host_out = [torch.empty(out_elems, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    host_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
     off = 0
     for p, xs, res, w, outs in calls:          # the step's inputs, packed
         for t in (*xs, res, w):
@@ -639,23 +670,26 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     slots = []
     for _ in range(2):
         dev_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-        dev_out = torch.empty(out_elems, dtype=torch.bfloat16, device=dev)
-        views, oi, oo = [], 0, 0
+        dev_out = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+        views, cur = [], {"in": 0, "out": 0}
 
-        def take(nbytes, dtype, shape):
-            nonlocal oi
-            t = dev_in[oi:oi + nbytes].view(dtype).view(*shape)
-            oi += nbytes
+        def take(buf, key, nbytes, dtype, shape):
+            t = buf[cur[key]:cur[key] + nbytes].view(dtype).view(*shape)
+            cur[key] += nbytes
             return t
         for p in problems:
             n = p.T * p.H
             xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
-            xs = [take(n * p.partial_bytes, xdt, (p.T, p.H)) for _ in range(p.W)]
-            res = take(n * 2, torch.bfloat16, (p.T, p.H))
-            w = take(p.H * 2, torch.bfloat16, (p.H,))
-            outs = tuple(dev_out[oo + k * n: oo + (k + 1) * n].view(p.T, p.H) for k in range(3))
-            oo += 3 * n
-            views.append((p, xs, res, w, outs))
+            xs = [take(dev_in, "in", n * p.partial_bytes, xdt, (p.T, p.H)) for _ in range(p.W)]
+            res = take(dev_in, "in", n * 2, torch.bfloat16, (p.T, p.H))
+            w = take(dev_in, "in", p.H * 2, torch.bfloat16, (p.H,))
+            outs = [take(dev_out, "out", n * 2, torch.bfloat16, (p.T, p.H)) for _ in range(2)]
+            outs.append(take(dev_out, "out", n * 2, torch.bfloat16, (p.T, p.H))
+                        if p.norm_out else None)
+            if p.fp8_out:
+                outs.append(take(dev_out, "out", n, torch.uint8, (p.T, p.H)))
+                outs.append(take(dev_out, "out", 4 * p.T, torch.float32, (p.T,)))
+            views.append((p, xs, res, w, tuple(outs)))
         slots.append((dev_in, dev_out, views))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     s_comp = stream
@@ -674,7 +708,7 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
         s_comp.wait_event(ev["in"][j])
         s_comp.wait_event(ev["out"][j])            # slot's outputs copied out
         for p, xs, res, w, outs in views:
-            farn.forward(xs, res, w, p.eps, out=outs, stream=s_comp)
+            call_forward(p, xs, res, w, outs, None, s_comp)
         ev["comp"][j].record(s_comp)
         s_out.wait_event(ev["comp"][j])
         with torch.cuda.stream(s_out):
@@ -705,7 +739,7 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     # the last step's outputs really came back
     assert torch.equal(host_out[(Ke - 1) % 2][-8:], slots[(Ke - 1) % 2][1][-8:].cpu())
     return {"value": world * step_bytes * Ke / (ms / 1e3) / 1e9, "unit": UNIT,
-            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_elems * 2,
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
             "steps": Ke, "ms_per_step": ms / Ke,
             "path": "per step: one pinned-host -> device copy of all inputs, "
                     "farn_forward for every call (C ABI via the Python binding), one "

@@ -199,9 +199,39 @@ int farn_forward_noalloc(int device,
                          void *reduced_out, void *residual_out, void *norm_out,
                          cudaStream_t stream, int *status_out);
 
-/* farn_plan for partials of type `partial_dtype` (a farn_dtype); fp32
- * partials are sized T*H*4 bytes in the aliasing checks. */
-int farn_plan_typed(const farn_ctx *ctx, int partial_dtype, int W, int64_t T, int64_t H,
+/* farn_forward_typed plus an FP8 copy of norm_out for the next layer's
+ * GEMM.  (The page does not describe this output; it extends the fused
+ * epilogue by one step.)  Per row t:
+ *     amax         = max over h of |norm_out[t,h]|   (the bf16 values; NaN ignored)
+ *     row_scale[t] = amax / 448, or 1 if amax is 0   (fp32; norm ~ q * scale)
+ *     norm_q[t,h]  = E4M3(norm_out[t,h] * inv),  inv = 448 / amax (fp32), or 1
+ * E4M3 is the OCP 8-bit float with 4 exponent and 3 fraction bits (largest
+ * finite 448, no infinities); the conversion rounds to nearest even and
+ * saturates larger magnitudes (and infinities) to +-448; NaN stays NaN.
+ *   norm_q     uint8 [T,H] (E4M3 patterns), 16-byte aligned for the fast
+ *              kernels
+ *   row_scale  float [T]
+ *   norm_out   bf16 [T,H], or NULL to skip writing it (it is still computed)
+ * The other arguments, checks and errors are those of farn_forward_typed;
+ * norm_q and row_scale take part in the aliasing checks. */
+int farn_forward_quant(const farn_ctx *ctx,
+                       const void *const *partials, int partial_dtype, int W,
+                       const void *residual, const void *weight, float eps,
+                       int64_t T, int64_t H,
+                       void *reduced_out, void *residual_out, void *norm_out,
+                       void *norm_q, float *row_scale,
+                       cudaStream_t stream);
+
+/* Flags of farn_plan_typed. */
+#define FARN_PLAN_FP8_OUT 1   /* the call also writes the FP8 norm output */
+
+/* farn_plan for partials of type `partial_dtype` (a farn_dtype), for a
+ * farn_forward_typed call (flags 0) or a farn_forward_quant call
+ * (FARN_PLAN_FP8_OUT; norm_out may then be NULL).  Only shape, dtype,
+ * flags and pointer alignment matter; aliasing is not checked.  Returns
+ * FARN_ERR_INVALID_ARG for a bad shape, dtype, flag or NULL pointer. */
+int farn_plan_typed(const farn_ctx *ctx, int partial_dtype, int flags, int W,
+                    int64_t T, int64_t H,
                     const void *const *partials, const void *residual,
                     const void *weight, const void *reduced_out,
                     const void *residual_out, const void *norm_out,

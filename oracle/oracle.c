@@ -214,10 +214,12 @@ int oracle_forward_f32(const float *const *x, int W, const uint16_t *residual,
  * 448 = 1.75 * 2^8; subnormals are multiples of 2^-9.
  *
  * Reading: per row t, amax = the largest |norm_out[t,h]| (NaN ignored, as
- * IEEE maxNum does), scale[t] = amax / 448 (fp32 division; 1 if amax is 0),
- * q[t,h] = E4M3(norm_out[t,h] / scale[t]) with round to nearest even and
- * saturation of any magnitude above 448 (infinity included) to 448; NaN
- * stays NaN.  Given the bf16 norm_out row, scale and q are unique.
+ * IEEE maxNum does); the scale written for dequantisation is
+ * scale[t] = amax / 448 and the quantised values use the row's fp32
+ * inverse inv = 448 / amax (both single fp32 divisions; 1 and 1 if amax is
+ * 0): q[t,h] = E4M3(norm_out[t,h] * inv), round to nearest even, any
+ * magnitude above 448 (infinity included) saturated to 448; NaN stays NaN.
+ * Given the bf16 norm_out row, scale and q are unique.
  * ------------------------------------------------------------------- */
 float oracle_e4m3_to_f32(uint8_t b)
 {
@@ -270,8 +272,9 @@ float oracle_quant_e4m3_row(const uint16_t *norm, int64_t H, uint8_t *q)
             amax = v;
     }
     float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
     for (int64_t h = 0; h < H; ++h)
-        q[h] = oracle_f32_to_e4m3_sat(oracle_bf16_to_f32(norm[h]) / scale);
+        q[h] = oracle_f32_to_e4m3_sat(oracle_bf16_to_f32(norm[h]) * inv);
     return scale;
 }
 

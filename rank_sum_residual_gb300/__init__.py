@@ -24,7 +24,8 @@ __all__ = [
     "FARN_MAX_W", "FarnError", "Context", "build_library", "library_path",
     "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
     "farn_plan", "farn_status_string", "farn_device_status", "farn_forward_noalloc",
-    "farn_forward_typed", "farn_plan_typed", "FARN_BF16", "FARN_F32",
+    "farn_forward_typed", "farn_plan_typed", "farn_forward_quant", "forward_quant",
+    "FARN_BF16", "FARN_F32",
     "forward", "VARIANTS",
 ]
 
@@ -66,6 +67,9 @@ def _load():
         lib.farn_forward_typed.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64,
                                            vp, vp, vp, vp]
         lib.farn_forward_typed.restype = i32
+        lib.farn_forward_quant.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64,
+                                           vp, vp, vp, vp, vp, vp]
+        lib.farn_forward_quant.restype = i32
         lib.farn_check_args.argtypes = [pvp, i32, cvp, cvp, f32, i64, i64,
                                         cvp, cvp, cvp]
         lib.farn_check_args.restype = i32
@@ -73,8 +77,8 @@ def _load():
                                   cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                   ctypes.POINTER(i32)]
         lib.farn_plan.restype = i32
-        lib.farn_plan_typed.argtypes = [vp, i32, i32, i64, i64, pvp, cvp, cvp, cvp, cvp,
-                                        cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+        lib.farn_plan_typed.argtypes = [vp, i32, i32, i32, i64, i64, pvp, cvp, cvp, cvp,
+                                        cvp, cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                         ctypes.POINTER(i32)]
         lib.farn_plan_typed.restype = i32
         lib.farn_forward_noalloc.argtypes = [i32, pvp, i32, cvp, cvp, f32, i64, i64,
@@ -137,6 +141,21 @@ def farn_forward_typed(ctx, partials, partial_dtype, W, residual, weight, eps, T
         ctypes.c_void_p(int(stream)))
 
 
+def farn_forward_quant(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                       reduced_out, residual_out, norm_out, norm_q, row_scale,
+                       stream=0) -> int:
+    """C ``farn_forward_quant``: also writes norm_out as E4M3 bytes plus a
+    per-row fp32 scale (norm_out may be 0 to skip it)."""
+    return _load().farn_forward_quant(
+        ctypes.c_void_p(ctx) if ctx else None, _ptr_array(partials), int(partial_dtype),
+        int(W), ctypes.c_void_p(int(residual)), ctypes.c_void_p(int(weight)), float(eps),
+        int(T), int(H), ctypes.c_void_p(int(reduced_out)),
+        ctypes.c_void_p(int(residual_out)),
+        ctypes.c_void_p(int(norm_out)) if norm_out else None,
+        ctypes.c_void_p(int(norm_q)), ctypes.c_void_p(int(row_scale)),
+        ctypes.c_void_p(int(stream)))
+
+
 def farn_forward_noalloc(device, partials, W, residual, weight, eps, T, H,
                          reduced_out, residual_out, norm_out, stream=0,
                          want_status=False):
@@ -188,12 +207,16 @@ def farn_plan(ctx, W, T, H, partials, residual, weight, reduced_out,
     return VARIANTS[variant.value], cs.value, thr.value
 
 
+FARN_PLAN_FP8_OUT = 1
+
+
 def farn_plan_typed(ctx, partial_dtype, W, T, H, partials, residual, weight, reduced_out,
-                    residual_out, norm_out):
+                    residual_out, norm_out, flags=0):
     """C ``farn_plan_typed``: (variant name, CTAs per row, threads per CTA)."""
     variant, cs, thr = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
-    st = _load().farn_plan_typed(ctypes.c_void_p(ctx), int(partial_dtype), int(W), int(T),
+    st = _load().farn_plan_typed(ctypes.c_void_p(ctx), int(partial_dtype), int(flags),
+                                 int(W), int(T),
                                  int(H), _ptr_array(partials), v(residual), v(weight),
                                  v(reduced_out), v(residual_out), v(norm_out),
                                  ctypes.byref(variant), ctypes.byref(cs), ctypes.byref(thr))
@@ -293,3 +316,39 @@ def forward(partials, residual, weight, eps: float, out=None, ctx=None,
     if st != FARN_OK:
         raise FarnError(st, "farn_forward")
     return out
+
+
+def forward_quant(partials, residual, weight, eps: float, write_norm: bool = True,
+                  ctx=None, stream=None):
+    """``forward`` plus the FP8 (E4M3) copy of norm_out and its per-row
+    scales.  Returns (reduced, residual_out, norm_out or None, norm_q as a
+    uint8 tensor of E4M3 patterns, row_scale float32 [T])."""
+    import torch
+    partials = list(partials)
+    if not partials:
+        raise ValueError("partials must hold at least one tensor")
+    T, H = residual.shape
+    dev = residual.device
+    pdt = partials[0].dtype
+    if pdt not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"partials must be bfloat16 or float32, got {pdt}")
+    for r, x in enumerate(partials):
+        _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
+    _check_tensor(residual, "residual", (T, H), dev)
+    _check_tensor(weight, "weight", (H,), dev)
+    red = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    nrm = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None
+    q = torch.empty((T, H), dtype=torch.uint8, device=dev)
+    scale = torch.empty((T,), dtype=torch.float32, device=dev)
+    c = ctx if ctx is not None else _context_for(dev.index)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = farn_forward_quant(c.handle, [x.data_ptr() for x in partials],
+                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
+                            residual.data_ptr(), weight.data_ptr(), eps, T, H,
+                            red.data_ptr(), ro.data_ptr(), nrm.data_ptr() if nrm is not None else 0,
+                            q.data_ptr(), scale.data_ptr(), s.cuda_stream)
+    if st != FARN_OK:
+        raise FarnError(st, "farn_forward_quant")
+    return red, ro, nrm, q, scale
+

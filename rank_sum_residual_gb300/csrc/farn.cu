@@ -45,7 +45,7 @@ struct farn_ctx {
   int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
   int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
   int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
-  int stage_regs[2];   // registers per thread of the stage kernels [4 vectors per thread]
+  int stage_regs[2][2];  // registers per thread of the stage kernels [FP8 output][4 vectors]
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
 };
@@ -57,17 +57,23 @@ typedef void (*VecKernel)(const farn::Params);
 // Chunks in flight per thread that the stage kernels are built for.
 constexpr int kStageDepths[3] = {16, 12, 8};
 
-VecKernel pick_stage(int vpt, int r) {
+template <bool Q>
+VecKernel pick_stage_q(int vpt, int r) {
   if (vpt == 2) {
-    if (r == 8) return &farn::farn_stage_kernel<2, 8>;
-    if (r == 12) return &farn::farn_stage_kernel<2, 12>;
-    if (r == 16) return &farn::farn_stage_kernel<2, 16>;
+    if (r == 8) return &farn::farn_stage_kernel<2, 8, Q>;
+    if (r == 12) return &farn::farn_stage_kernel<2, 12, Q>;
+    if (r == 16) return &farn::farn_stage_kernel<2, 16, Q>;
   } else if (vpt == 4) {
-    if (r == 8) return &farn::farn_stage_kernel<4, 8>;
-    if (r == 12) return &farn::farn_stage_kernel<4, 12>;
-    if (r == 16) return &farn::farn_stage_kernel<4, 16>;
+    if (r == 8) return &farn::farn_stage_kernel<4, 8, Q>;
+    if (r == 12) return &farn::farn_stage_kernel<4, 12, Q>;
+    if (r == 16) return &farn::farn_stage_kernel<4, 16, Q>;
   }
   return nullptr;
+}
+
+// quant: the instantiation that also writes the FP8 output
+VecKernel pick_stage(int vpt, int r, bool quant = false) {
+  return quant ? pick_stage_q<true>(vpt, r) : pick_stage_q<false>(vpt, r);
 }
 
 VecKernel pick_generic(int pb) {
@@ -194,12 +200,13 @@ int choose_vpt(int64_t sv) {
 //      that give >= 320 threads per SM and fit registers and shared memory;
 //   2. else one CTA per SM, 2 then 4 vectors per thread;
 // each with the largest of 16 / 12 / 8 chunks in flight per thread that fits.
-bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T) {
+bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T,
+               bool quant) {
   if (ctx->force_vpt > 0 && ctx->force_vpt != vpt) return false;
   if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
   const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
   if (nt > 512) return false;
-  const int regs = ctx->stage_regs[vpt >= 4];
+  const int regs = ctx->stage_regs[quant][vpt >= 4];
   if ((int64_t)regs * nt * ctas > 65536) return false;
   const size_t budget = (size_t)ctx->max_smem / (size_t)ctas - 1024;
   int r = 0;
@@ -222,31 +229,34 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
 }
 
 // bf16 partials only (fp32 partials take the row kernel, see the kernel).
-bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
+bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, bool quant) {
   const int64_t hv = H / 8;
   const int vpts[2] = {4, 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
-    return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T) ||
-           stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T);
+    return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, quant) ||
+           stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T, quant);
   for (int i = 0; i < 2; ++i) {
     const int vpt = vpts[i];
     const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
     int ctas = (int)((320 + nt - 1) / nt);
     if (ctas < 2) ctas = 2;
     for (; ctas <= 4; ++ctas)
-      if (stage_fit(ctx, hv, vpt, ctas, pl, T)) return true;
+      if (stage_fit(ctx, hv, vpt, ctas, pl, T, quant)) return true;
   }
-  return stage_fit(ctx, hv, 2, 1, pl, T) || stage_fit(ctx, hv, 4, 1, pl, T);
+  return stage_fit(ctx, hv, 2, 1, pl, T, quant) || stage_fit(ctx, hv, 4, 1, pl, T, quant);
 }
 
-int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out) {
+int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
+              bool quant = false) {
   Plan pl;
   pl.pb = pb;
+  // The FP8 output is produced by every kernel but the TMA-staged one.
+  if (quant && ctx->force_variant == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
   const bool small = T < ctx->small_t;
   pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
-  if (vec_ok && pb == 2 && (want == kVariantBulk ||
+  if (vec_ok && pb == 2 && !quant && (want == kVariantBulk ||
                  (want == kVariantAuto && ctx->bulk && !small && ctx->force_cluster == 0)) &&
       make_bulk_plan(ctx, T, H, &pl)) {
     *out = pl;
@@ -257,7 +267,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
                   ctx->force_cluster == 0)) &&
-      make_stage_plan(ctx, T, H, &pl)) {
+      make_stage_plan(ctx, T, H, &pl, quant)) {
     *out = pl;
     return FARN_OK;
   }
@@ -340,30 +350,37 @@ const char* farn_status_string(int status) {
 
 namespace {
 
-// The argument checks for partials of `pb` bytes per element.
+// The argument checks for partials of `pb` bytes per element; with an FP8
+// output (q_out [T,H] bytes and scale_out [T] floats, both non-null)
+// norm_out may be null.
 int check_args_pb(const void* const* partials, int W, int pb, const void* residual,
                   const void* weight, float eps, int64_t T, int64_t H,
-                  const void* reduced_out, const void* residual_out, const void* norm_out) {
+                  const void* reduced_out, const void* residual_out, const void* norm_out,
+                  const void* q_out = nullptr, const void* scale_out = nullptr,
+                  bool quant = false) {
   if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1) return FARN_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
   if (H > INT64_MAX / 4 || (T > 0 && T > INT64_MAX / (4 * H))) return FARN_ERR_INVALID_ARG;
   // With no rows nothing is read or written: empty tensors may have null
   // data pointers.
   if (T == 0) return FARN_OK;
-  if (!residual || !weight || !reduced_out || !residual_out || !norm_out)
+  if (!residual || !weight || !reduced_out || !residual_out || (!norm_out && !quant))
     return FARN_ERR_INVALID_ARG;
+  if (quant && (!q_out || !scale_out)) return FARN_ERR_INVALID_ARG;
   for (int r = 0; r < W; ++r)
     if (!partials[r]) return FARN_ERR_INVALID_ARG;
   const int64_t nb = T * H * 2, xb = T * H * pb, wb = H * 2;
-  const void* outs[3] = {reduced_out, residual_out, norm_out};
-  for (int i = 0; i < 3; ++i) {
-    for (int j = i + 1; j < 3; ++j)
-      if (overlaps(outs[i], nb, outs[j], nb)) return FARN_ERR_ALIAS;
+  // outputs and their byte extents (a null norm_out extends over nothing)
+  const void* outs[5] = {reduced_out, residual_out, norm_out, q_out, scale_out};
+  const int64_t ob[5] = {nb, nb, norm_out ? nb : 0, quant ? T * H : 0, quant ? T * 4 : 0};
+  for (int i = 0; i < 5; ++i) {
+    for (int j = i + 1; j < 5; ++j)
+      if (overlaps(outs[i], ob[i], outs[j], ob[j])) return FARN_ERR_ALIAS;
     for (int r = 0; r < W; ++r)
-      if (overlaps(outs[i], nb, partials[r], xb)) return FARN_ERR_ALIAS;
-    if (overlaps(outs[i], nb, weight, wb)) return FARN_ERR_ALIAS;
+      if (overlaps(outs[i], ob[i], partials[r], xb)) return FARN_ERR_ALIAS;
+    if (overlaps(outs[i], ob[i], weight, wb)) return FARN_ERR_ALIAS;
     const bool inplace_residual = (i == 1 && residual_out == residual);
-    if (!inplace_residual && overlaps(outs[i], nb, residual, nb)) return FARN_ERR_ALIAS;
+    if (!inplace_residual && overlaps(outs[i], ob[i], residual, nb)) return FARN_ERR_ALIAS;
   }
   return FARN_OK;
 }
@@ -466,10 +483,10 @@ int farn_create(farn_ctx** out, int device) {
   }
   memset(c->stage_regs, 0, sizeof c->stage_regs);
   for (int vpt = 2; vpt <= 4; vpt *= 2) {
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 6; ++i) {
       // dynamic + static shared memory may not exceed the opt-in limit
       cudaFuncAttributes fa;
-      const void* k = (const void*)pick_stage(vpt, kStageDepths[i]);
+      const void* k = (const void*)pick_stage(vpt, kStageDepths[i % 3], i >= 3);
       if (cudaFuncGetAttributes(&fa, k) != cudaSuccess ||
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {
@@ -477,7 +494,7 @@ int farn_create(farn_ctx** out, int device) {
         cudaGetLastError();
         return FARN_ERR_CUDA;
       }
-      int& regs = c->stage_regs[vpt >= 4];
+      int& regs = c->stage_regs[i >= 3][vpt >= 4];
       if (fa.numRegs > regs) regs = fa.numRegs;
     }
   }
@@ -543,25 +560,30 @@ int farn_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, const void* cons
               const void* residual, const void* weight, const void* reduced_out,
               const void* residual_out, const void* norm_out, int* variant,
               int* cluster_size, int* threads) {
-  return farn_plan_typed(ctx, FARN_BF16, W, T, H, partials, residual, weight, reduced_out,
+  return farn_plan_typed(ctx, FARN_BF16, 0, W, T, H, partials, residual, weight, reduced_out,
                          residual_out, norm_out, variant, cluster_size, threads);
 }
 
-int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int W, int64_t T, int64_t H,
-                    const void* const* partials, const void* residual, const void* weight,
-                    const void* reduced_out, const void* residual_out, const void* norm_out,
-                    int* variant, int* cluster_size, int* threads) {
+int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int flags, int W, int64_t T,
+                    int64_t H, const void* const* partials, const void* residual,
+                    const void* weight, const void* reduced_out, const void* residual_out,
+                    const void* norm_out, int* variant, int* cluster_size, int* threads) {
   if (!ctx || !variant || !cluster_size || !threads) return FARN_ERR_INVALID_ARG;
   const int pb = dtype_bytes(partial_dtype);
-  if (!pb) return FARN_ERR_INVALID_ARG;
-  int st = check_args_pb(partials, W, pb, residual, weight, 1.0f, T, H, reduced_out,
-                         residual_out, norm_out);
-  if (st != FARN_OK) return st;
+  if (!pb || (flags & ~FARN_PLAN_FP8_OUT)) return FARN_ERR_INVALID_ARG;
+  const bool quant = (flags & FARN_PLAN_FP8_OUT) != 0;
+  // The choice depends on the shape, the dtype, the FP8 flag and the
+  // pointers' alignment only; aliasing is not checked here.
+  if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1 || !residual || !weight ||
+      !reduced_out || !residual_out || (!norm_out && !quant))
+    return FARN_ERR_INVALID_ARG;
+  for (int r = 0; r < W; ++r)
+    if (!partials[r]) return FARN_ERR_INVALID_ARG;
   Plan pl;
-  st = make_plan(ctx, T, H,
+  int st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
-                                norm_out, H),
-                 pb, &pl);
+                                norm_out ? norm_out : reduced_out, H),
+                 pb, &pl, quant);
   if (st != FARN_OK) return st;
   *variant = pl.variant;
   *cluster_size = pl.cs;
@@ -577,15 +599,17 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
                             reduced_out, residual_out, norm_out, stream);
 }
 
-int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
-                       int W, const void* residual, const void* weight, float eps, int64_t T,
-                       int64_t H, void* reduced_out, void* residual_out, void* norm_out,
-                       cudaStream_t stream) {
+// farn_forward_typed and farn_forward_quant: q_out/scale_out and quant only
+// for the FP8 output.
+static int forward_impl(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
+                        int W, const void* residual, const void* weight, float eps, int64_t T,
+                        int64_t H, void* reduced_out, void* residual_out, void* norm_out,
+                        void* q_out, float* scale_out, bool quant, cudaStream_t stream) {
   if (!ctx) return FARN_ERR_INVALID_ARG;
   const int pb = dtype_bytes(partial_dtype);
   if (!pb) return FARN_ERR_INVALID_ARG;
   int st = check_args_pb(partials, W, pb, residual, weight, eps, T, H, reduced_out,
-                         residual_out, norm_out);
+                         residual_out, norm_out, q_out, scale_out, quant);
   if (st != FARN_OK) return st;
   if (T == 0) return FARN_OK;
   if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
@@ -594,8 +618,9 @@ int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int par
   Plan pl;
   st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
-                                norm_out, H),
-                 pb, &pl);
+                                norm_out ? norm_out : reduced_out, H) &&
+                     (!quant || ((uintptr_t)q_out & 15u) == 0),
+                 pb, &pl, quant);
   if (st != FARN_OK) return st;
 
   farn::Params prm;
@@ -606,6 +631,8 @@ int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int par
   prm.reduced = reduced_out;
   prm.residual_out = residual_out;
   prm.norm_out = norm_out;
+  prm.q_out = static_cast<uint8_t*>(q_out);
+  prm.scale_out = scale_out;
   prm.T = T;
   prm.H = H;
   prm.W = W;
@@ -649,7 +676,7 @@ int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int par
   } else if (pl.variant == kVariantBulk) {
     err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm);
   } else if (pl.variant == kVariantStage) {
-    err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r), prm);
+    err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r, quant), prm);
   } else {
     VecKernel k = pick_vec(pl.vpt, pl.cs, pb);
     err = cudaLaunchKernelEx(&cfg, k, prm);
@@ -659,6 +686,22 @@ int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int par
     return FARN_ERR_CUDA;
   }
   return FARN_OK;
+}
+
+int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
+                       int W, const void* residual, const void* weight, float eps, int64_t T,
+                       int64_t H, void* reduced_out, void* residual_out, void* norm_out,
+                       cudaStream_t stream) {
+  return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                      reduced_out, residual_out, norm_out, nullptr, nullptr, false, stream);
+}
+
+int farn_forward_quant(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
+                       int W, const void* residual, const void* weight, float eps, int64_t T,
+                       int64_t H, void* reduced_out, void* residual_out, void* norm_out,
+                       void* norm_q, float* row_scale, cudaStream_t stream) {
+  return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                      reduced_out, residual_out, norm_out, norm_q, row_scale, true, stream);
 }
 
 // ------------------------------------------------------------------------

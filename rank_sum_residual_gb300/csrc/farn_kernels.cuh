@@ -44,6 +44,10 @@ struct Params {
   int64_t H;     // elements per row
   int W;         // partials
   float eps;
+  // optional FP8 (E4M3) output of norm_out, row kernels only: q_out [T,H]
+  // bytes and scale_out [T] fp32, or null; norm_out may then be null too
+  uint8_t* q_out;
+  float* scale_out;
   // bulk (TMA-staged) kernel only
   int* err;               // device status word, bits of kBulkErr* on a timeout
   uint32_t stages;        // shared-memory ring stages
@@ -65,6 +69,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ uint16_t to_bf16(float v) {
   return (uint16_t)(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+}
+
+// Two fp32 values to E4M3 (round to nearest even, finite saturation),
+// lo in the low byte.  One cvt.rn.satfinite.e4m3x2.f32.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
+}
+
+// The per-row FP8 scale written for dequantisation, amax / 448, and the
+// inverse the values are multiplied by, 448 / amax (each one IEEE fp32
+// division per row; both 1 for an all-zero row).
+__device__ __forceinline__ float e4m3_row_scale(float amax) {
+  return amax > 0.0f ? amax / 448.0f : 1.0f;
+}
+__device__ __forceinline__ float e4m3_row_inv(float amax) {
+  return amax > 0.0f ? 448.0f / amax : 1.0f;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
 }
 
 // ----------------------------------------------------------- memory access
@@ -179,6 +207,8 @@ farn_vec_kernel(const __grid_constant__ Params p) {
 
   __shared__ float warp_ss[2][32];
   __shared__ float cluster_ss[2][CS];   // [row parity][CTA rank in cluster]
+  __shared__ float warp_mx[2][32];      // FP8 output only: row amax
+  __shared__ float cluster_mx[2][CS];
 
   const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
   // Small slices (decode-sized calls) are latency bound: their weight is
@@ -309,9 +339,12 @@ farn_vec_kernel(const __grid_constant__ Params p) {
     // a4: rstd with IEEE division and square root, then the normalised,
     // weighted output.
     const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+    uint4 nb[VPT];
+    float mx = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int j = tid + k * blockDim.x;
+      nb[k] = make_uint4(0u, 0u, 0u, 0u);
       if (j < sv) {
         const uint32_t q[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
         const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
@@ -321,10 +354,47 @@ farn_vec_kernel(const __grid_constant__ Params p) {
           const float n0 = (bf_lo(q[e]) * rstd) * bf_lo(w[e]);
           const float n1 = (bf_hi(q[e]) * rstd) * bf_hi(w[e]);
           n[e] = pack_bf16x2(n0, n1);
+          mx = fmaxf(mx, fmaxf(fabsf(bf_lo(n[e])), fabsf(bf_hi(n[e]))));
         }
-        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
-                  make_uint4(n[0], n[1], n[2], n[3]));
+        nb[k] = make_uint4(n[0], n[1], n[2], n[3]);
+        if (p.norm_out) st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j, nb[k]);
       }
+    }
+
+    if (p.q_out) {
+      // FP8 output: the row's amax of the bf16 norm_out (fmaxf ignores NaN;
+      // max is exact, so every CTA and thread gets the same value), then
+      // E4M3(norm_out * (448 / amax)) for each element.
+      mx = warp_max(mx);
+      float* wm = warp_mx[it & 1];
+      if (lane == 0) wm[warp] = mx;
+      __syncthreads();
+      float amax = 0.0f;
+      for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, wm[w]);
+      if (CS > 1) {
+        float* slots = cluster_mx[it & 1];
+        if (tid < CS) st_dsmem_f32(&slots[slice], (uint32_t)tid, amax);
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        for (int c = 0; c < CS; ++c) amax = fmaxf(amax, slots[c]);
+      }
+      const float scale = e4m3_row_scale(amax);
+      const float inv = e4m3_row_inv(amax);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * blockDim.x;
+        if (j < sv) {
+          const uint32_t n[4] = {nb[k].x, nb[k].y, nb[k].z, nb[k].w};
+          uint32_t q8[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            q8[e] = pack_e4m3x2(bf_lo(n[e]) * inv, bf_hi(n[e]) * inv);
+          const uint2 out = make_uint2(q8[0] | (q8[1] << 16), q8[2] | (q8[3] << 16));
+          asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};"
+                       :: "l"(p.q_out + (base + j) * 8), "r"(out.x), "r"(out.y) : "memory");
+        }
+      }
+      if (tid == 0 && slice == 0) p.scale_out[row] = scale;
     }
   }
 }
@@ -374,10 +444,33 @@ farn_generic_kernel(const __grid_constant__ Params p) {
     float tot = 0.0f;
     for (int w = 0; w < nwarps; ++w) tot += ws[w];
     const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+    float mx = 0.0f;
     for (int64_t h = tid; h < p.H; h += blockDim.x) {
       const float q = __uint_as_float((uint32_t)ro_out[off + h] << 16);
       const float w = __uint_as_float((uint32_t)wt[h] << 16);
-      nrm_out[off + h] = to_bf16((q * rstd) * w);
+      const uint16_t nbits = to_bf16((q * rstd) * w);
+      if (nrm_out) nrm_out[off + h] = nbits;
+      mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)nbits << 16)));
+    }
+    if (p.q_out) {
+      // FP8 output: row amax, then a third pass that recomputes each
+      // normalised value (same arithmetic, same bits) and quantises it.
+      __shared__ float warp_mx[2][32];
+      mx = warp_max(mx);
+      float* wm = warp_mx[it & 1];
+      if (lane == 0) wm[warp] = mx;
+      __syncthreads();
+      float amax = 0.0f;
+      for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, wm[w]);
+      const float scale = e4m3_row_scale(amax);
+      const float inv = e4m3_row_inv(amax);
+      for (int64_t h = tid; h < p.H; h += blockDim.x) {
+        const float q = __uint_as_float((uint32_t)ro_out[off + h] << 16);
+        const float w = __uint_as_float((uint32_t)wt[h] << 16);
+        const float n = __uint_as_float((uint32_t)to_bf16((q * rstd) * w) << 16);
+        p.q_out[off + h] = (uint8_t)(pack_e4m3x2(n * inv, 0.0f) & 0xFFu);
+      }
+      if (tid == 0) p.scale_out[row] = scale;
     }
   }
 }
@@ -686,7 +779,10 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
-template <int VPT, int R>
+// QUANT: also write the FP8 copy of norm_out (p.q_out, p.scale_out; p.norm_out
+// may be null), as farn_vec_kernel does; compiled separately so the plain
+// kernel is unchanged.
+template <int VPT, int R, bool QUANT = false>
 __global__ void __launch_bounds__(512)
 farn_stage_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -698,6 +794,7 @@ farn_stage_kernel(const __grid_constant__ Params p) {
   const int W = p.W;
   const float Hf = (float)p.H;
   __shared__ float warp_ss[2][32];
+  __shared__ float warp_mx[2][32];      // FP8 output only: row amax
   const uint32_t slots = (uint32_t)__cvta_generic_to_shared(smem);
   // slot s, vector k of this thread
   auto slot_addr = [&](int s, int k) -> uint32_t {
@@ -799,6 +896,8 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     float tot = 0.0f;
     for (int w = 0; w < nwarps; ++w) tot += ws[w];
     const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+    uint4 nb[VPT];
+    float mx = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int j = tid + k * nt;
@@ -811,10 +910,39 @@ farn_stage_kernel(const __grid_constant__ Params p) {
           const float n0 = (bf_lo(qv[e]) * rstd) * bf_lo(w[e]);
           const float n1 = (bf_hi(qv[e]) * rstd) * bf_hi(w[e]);
           n[e] = pack_bf16x2(n0, n1);
+          if constexpr (QUANT) mx = fmaxf(mx, fmaxf(fabsf(bf_lo(n[e])), fabsf(bf_hi(n[e]))));
         }
-        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
-                  make_uint4(n[0], n[1], n[2], n[3]));
+        if constexpr (QUANT) nb[k] = make_uint4(n[0], n[1], n[2], n[3]);
+        if (!QUANT || p.norm_out)
+          st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                    make_uint4(n[0], n[1], n[2], n[3]));
       }
+    }
+    if constexpr (QUANT) {
+      // the row's amax (exact, NaN ignored), then E4M3(norm * 448 / amax)
+      mx = warp_max(mx);
+      float* wm = warp_mx[it & 1];
+      if (lane == 0) wm[warp] = mx;
+      __syncthreads();
+      float amax = 0.0f;
+      for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, wm[w]);
+      const float scale = e4m3_row_scale(amax);
+      const float inv = e4m3_row_inv(amax);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * nt;
+        if (j < hv) {
+          const uint32_t n[4] = {nb[k].x, nb[k].y, nb[k].z, nb[k].w};
+          uint32_t q8[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            q8[e] = pack_e4m3x2(bf_lo(n[e]) * inv, bf_hi(n[e]) * inv);
+          asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};"
+                       :: "l"(p.q_out + (base + j) * 8), "r"(q8[0] | (q8[1] << 16)),
+                          "r"(q8[2] | (q8[3] << 16)) : "memory");
+        }
+      }
+      if (tid == 0) p.scale_out[row] = scale;
     }
   }
   cp_async_wait<0>();   // nothing may land after the CTA exits

@@ -71,25 +71,38 @@ class Problem:
     residual: Dist = Dist(NORMAL, 0.0, 1.0)
     weight: Dist = Dist(NORMAL, 1.0, 0.1)
     partial_dtype: str = "bf16"      # or "f32"
+    fp8_out: bool = False            # also write norm_out as E4M3 + row scales
+    norm_out: bool = True            # write the bf16 norm_out
 
     @property
     def partial_bytes(self) -> int:
         return 4 if self.partial_dtype == "f32" else 2
 
+    def read_bytes(self) -> int:
+        """W*T*H*pb partials + T*H*2 residual + H*2 weight (pb = 2 for bf16
+        partials, 4 for fp32)."""
+        return self.W * self.T * self.H * self.partial_bytes + self.T * self.H * 2 + self.H * 2
+
+    def write_bytes(self) -> int:
+        """reduced and residual_out (T*H*2 each), norm_out (T*H*2) if
+        written, and with the FP8 output T*H bytes plus T*4 of scales."""
+        n = self.T * self.H
+        return 2 * n * 2 + (n * 2 if self.norm_out else 0) + \
+            ((n + 4 * self.T) if self.fp8_out else 0)
+
     def algorithmic_bytes(self) -> int:
-        """W*T*H*pb partials + T*H*2 residual + H*2 weight read, 3*T*H*2
-        written (pb = 2 for bf16 partials, 4 for fp32)."""
-        return (self.W * self.T * self.H * self.partial_bytes + self.T * self.H * 2
-                + self.H * 2 + 3 * self.T * self.H * 2)
+        return self.read_bytes() + self.write_bytes()
+
+    def _replace(self, **kw) -> "Problem":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return Problem(**d)
 
     def with_seed(self, seed: int) -> "Problem":
-        return Problem(self.name, self.W, self.T, self.H, self.eps, seed,
-                       self.x, self.residual, self.weight, self.partial_dtype)
+        return self._replace(seed=seed)
 
     def with_T(self, T: int) -> "Problem":
-        return Problem(f"{self.name.split('@')[0]}@T{T}", self.W, T, self.H,
-                       self.eps, self.seed, self.x, self.residual, self.weight,
-                       self.partial_dtype)
+        return self._replace(name=f"{self.name.split('@')[0]}@T{T}", T=T)
 
 
 N01 = Dist(NORMAL, 0.0, 1.0)
@@ -110,6 +123,10 @@ WORKLOADS = {
     "wide": [Problem("wide", 16, 4096, 7168, 1e-6, 0, Dist(NORMAL, 0.0, 1.0 / 16))],
     # residual add + RMSNorm alone (one partial: no rank sum), prefill-sized
     "rmsnorm": [Problem("rmsnorm", 1, 8192, 8192, 1e-6, 0, N01)],
+    # the prefill shape writing norm_out as E4M3 + row scales instead of bf16
+    "prefill_fp8": [Problem("prefill_fp8", 8, 8192, 8192, 1e-6, 0,
+                            Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
+                            N01, Dist(UNIFORM, 0.5, 1.5), fp8_out=True, norm_out=False)],
     # the prefill shape with fp32 partials (e.g. straight from GEMM epilogues)
     "prefill_f32": [Problem("prefill_f32", 8, 8192, 8192, 1e-6, 0,
                             Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),

@@ -451,7 +451,7 @@ def pin_e4m3_matches_torch_cast(O):
 
 def pin_quant_row_closed_forms(O):
     one = bx.bits(1)
-    # [1, -2, 0.5, 0]: amax 2, scale 2/448, values map to 224, -448, 112, 0
+    # [1, -2, 0.5, 0]: amax 2, scale 2/448, inv 224, values map to 224, -448, 112, 0
     row = np.array([bx.bits(1), bx.bits(-2), bx.bits(0.5), 0], np.uint16)
     q, sc = O.quant_e4m3(row)
     assert abs(sc[0] - np.float32(2) / np.float32(448)) == 0
@@ -487,8 +487,9 @@ def pin_quant_row_power_of_two_invariance(O):
         assert np.array_equal(q0, q1) and np.array_equal(s1, s0 * np.float32(2.0 ** k))
 
 
-def pin_quant_row_vs_exact_division(O):
-    """q = E4M3(x / scale) with the division rounded to fp32 first."""
+def pin_quant_row_vs_exact_rounding(O):
+    """q = E4M3(x * inv), inv = 448 / amax rounded to fp32, the product
+    rounded to fp32 first; scale = amax / 448 rounded to fp32."""
     rng = np.random.default_rng(43)
     rows = (rng.normal(size=(8, 48)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
     q, sc = O.quant_e4m3(rows)
@@ -496,9 +497,10 @@ def pin_quant_row_vs_exact_division(O):
         vals = bx.to_f64(rows[t])
         amax = np.float32(np.abs(vals).max())
         scale = np.float32(amax / np.float32(448))
+        inv = np.float32(np.float32(448) / amax)
         assert sc[t] == scale
         for h in range(48):
-            d = np.float32(np.float32(vals[h]) / scale)
+            d = np.float32(np.float32(vals[h]) * inv)
             assert int(q[t][h]) == e4m3_exact(Fraction(float(d)) if d != 0 else float(d))
 
 

@@ -79,7 +79,7 @@ def test_reference_arm_json_line(monkeypatch):
 def test_algorithmic_bytes_formula(name):
     for p in synth.workload(name):
         read = p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
-        write = 3 * p.T * p.H * 2
+        write = (2 + p.norm_out) * p.T * p.H * 2 + (p.T * p.H + 4 * p.T) * p.fp8_out
         assert p.algorithmic_bytes() == read + write
         assert bench.call_bytes(p, p.T) == read + write
 

@@ -108,6 +108,12 @@ def test_adjacent_buffers_are_not_aliases():
 def test_forward_rejects_null_context_before_any_cuda_call():
     st = farn.farn_forward(0, X[:4], 4, RES, WT, 1e-6, 4, 64, RED, RO, NRM, 0)
     assert st == farn.FARN_ERR_INVALID_ARG
+    st = farn.farn_forward_typed(0, X[:4], farn.FARN_F32, 4, RES, WT, 1e-6, 4, 64,
+                                 RED, RO, NRM, 0)
+    assert st == farn.FARN_ERR_INVALID_ARG
+    st = farn.farn_forward_quant(0, X[:4], farn.FARN_BF16, 4, RES, WT, 1e-6, 4, 64,
+                                 RED, RO, NRM, 0x25000000, 0x26000000, 0)
+    assert st == farn.FARN_ERR_INVALID_ARG
 
 
 def test_create_without_a_gpu_reports_cuda_error():

@@ -615,6 +615,14 @@ def test_f32_partials_plan(dev):
         assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 2, 4096, *args)[0] == "cluster"
         with pytest.raises(farn.FarnError):
             farn.farn_plan_typed(c.handle, 7, 8, 2, 4096, *args)
+        # with the FP8 output (norm_out written or not) the same kernel choice
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 8192, *args,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
+        noq = args[:5] + (0,)
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 8192, *noq,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 8192, 8192, *noq,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "row"
     finally:
         c.close()
 
@@ -672,3 +680,111 @@ def test_two_streams_concurrently(O, dev):
     for oa, ob in zip(outs_a, outs_b):
         assert_parity([u16(t.index_select(0, idx)) for t in oa], want_a, "stream 1")
         assert_parity([u16(t) for t in ob], want_b, "stream 2")
+
+
+# ------------------------------------------------------ FP8 norm output
+def _check_quant(O, xs, res, w, eps, red, ro, nrm, q, scale, what):
+    """norm_out within 1 ulp of the oracle; given the GPU's norm_out, the
+    E4M3 bytes and the row scales are unique: bit-exact against the
+    oracle's quantisation of that norm_out (NaN by pattern class)."""
+    assert_parity([u16(red), u16(ro), u16(nrm)], oracle_rows(O, xs, res, w, eps), what)
+    want_q, want_s = O.quant_e4m3(u16(nrm))
+    got_q = q.cpu().numpy()
+    got_s = scale.cpu().numpy()
+    assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32)), what
+    nan_w = (want_q & 0x7F) == 0x7F
+    assert np.array_equal((got_q & 0x7F) == 0x7F, nan_w), what
+    assert np.array_equal(np.where(nan_w, 0, got_q), np.where(nan_w, 0, want_q)), what
+
+
+@pytest.mark.parametrize("name,T", [("decode", 1), ("decode", 5), ("decode", 64),
+                                    ("prefill", 300), ("prefill", 2200), ("wide", 100),
+                                    ("nonpow2", 77), ("prefill_f32", 9)])
+def test_fp8_output(O, dev, name, T):
+    p = synth.workload(name)[0].with_T(T)
+    xs, res, w = synth.device_inputs(p, dev)
+    red, ro, nrm, q, scale = farn.forward_quant(xs, res, w, p.eps)
+    torch.cuda.synchronize()
+    _check_quant(O, xs, res, w, p.eps, red, ro, nrm, q, scale, f"fp8 {name} T={T}")
+
+
+@pytest.mark.parametrize("env", [dict(FARN_VARIANT="generic"), dict(FARN_CLUSTER=2),
+                                 dict(FARN_CLUSTER=16), dict(FARN_VARIANT="row", FARN_VPT=4),
+                                 dict(FARN_VARIANT="stage"), dict(FARN_VARIANT="stage", FARN_VPT=2),
+                                 dict(FARN_VARIANT="stage", FARN_STAGE_CTAS=1)],
+                         ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
+def test_fp8_output_forced_variants(O, dev, env):
+    p = synth.Problem("q", 6, 7, 4096, 1e-6, 13, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    ctx = make_ctx(**env)
+    try:
+        red, ro, nrm, q, scale = farn.forward_quant(xs, res, w, p.eps, ctx=ctx)
+        torch.cuda.synchronize()
+        _check_quant(O, xs, res, w, p.eps, red, ro, nrm, q, scale, f"fp8 {env}")
+    finally:
+        ctx.close()
+
+
+def test_fp8_output_without_norm_out_and_specials(O, dev):
+    """norm_out not written: the same E4M3 bytes and scales as with it;
+    rows with a NaN, an overflow, all zeros and tiny values."""
+    W, T, H = 4, 6, 1000                 # H % 8 != 0: generic kernel
+    p = synth.Problem("q", W, T, H, 1e-6, 21, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    xs[1][0, 5] = float("nan")
+    for x in xs:
+        x[1, 7] = 3.0e38                 # reduced -> inf, the row's norm -> NaN
+        x[2].zero_()
+    res[2].zero_()
+    for x in xs:
+        x[3].view(torch.int16)[:] = 1    # 2^-133 everywhere
+    res[3].zero_()
+    red, ro, nrm, q, scale = farn.forward_quant(xs, res, w, p.eps)
+    red2, ro2, nrm2, q2, scale2 = farn.forward_quant(xs, res, w, p.eps, write_norm=False)
+    torch.cuda.synchronize()
+    assert nrm2 is None
+    _check_quant(O, xs, res, w, p.eps, red, ro, nrm, q, scale, "fp8 specials")
+    assert torch.equal(q, q2) and torch.equal(scale.view(torch.int32), scale2.view(torch.int32))
+    assert scale[2].item() == 1.0 and not q[2].any()      # zero row
+
+
+def test_fp8_output_vector_path_without_norm_out(O, dev):
+    p = synth.workload("prefill")[0].with_T(500)
+    xs, res, w = synth.device_inputs(p, dev)
+    a = farn.forward_quant(xs, res, w, p.eps)
+    b = farn.forward_quant(xs, res, w, p.eps, write_norm=False)
+    torch.cuda.synchronize()
+    _check_quant(O, xs, res, w, p.eps, *a, "fp8 with norm")
+    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
+
+
+@pytest.mark.parametrize("variant", ["bulk"])
+def test_fp8_output_refused_by_staged_kernels(dev, variant):
+    p = synth.Problem("q", 2, 4, 2048, 1e-6, 1, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    ctx = make_ctx(FARN_VARIANT=variant)
+    try:
+        with pytest.raises(farn.FarnError) as e:
+            farn.forward_quant(xs, res, w, p.eps, ctx=ctx)
+        assert e.value.status == farn.FARN_ERR_UNSUPPORTED
+    finally:
+        ctx.close()
+
+
+def test_fp8_output_aliasing(dev):
+    p = synth.Problem("q", 2, 4, 2048, 1e-6, 1, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    red, ro, nrm = (torch.empty_like(res) for _ in range(3))
+    scale = torch.empty(4, dtype=torch.float32, device=dev)
+    c = farn._context_for(0)
+    # the E4M3 output over the reduced output: refused
+    st = farn.farn_forward_quant(c.handle, [x.data_ptr() for x in xs], farn.FARN_BF16, 2,
+                                 res.data_ptr(), w.data_ptr(), p.eps, 4, 2048, red.data_ptr(),
+                                 ro.data_ptr(), nrm.data_ptr(), red.data_ptr(), scale.data_ptr())
+    assert st == farn.FARN_ERR_ALIAS
+    # a missing scale output: invalid
+    q = torch.empty((4, 2048), dtype=torch.uint8, device=dev)
+    st = farn.farn_forward_quant(c.handle, [x.data_ptr() for x in xs], farn.FARN_BF16, 2,
+                                 res.data_ptr(), w.data_ptr(), p.eps, 4, 2048, red.data_ptr(),
+                                 ro.data_ptr(), nrm.data_ptr(), q.data_ptr(), 0)
+    assert st == farn.FARN_ERR_INVALID_ARG

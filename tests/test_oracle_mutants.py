@@ -66,7 +66,8 @@ MUTANTS = {
     "e4m3_truncates": ("float k = rintf(a / step);", "float k = truncf(a / step);"),
     "e4m3_wrong_bias": ("(uint8_t)((E + 7) << 3)", "(uint8_t)((E + 8) << 3)"),
     "quant_scale_wrong_max": ("amax / 448.0f : 1.0f", "amax / 240.0f : 1.0f"),
-    "quant_multiplies": ("oracle_bf16_to_f32(norm[h]) / scale)", "oracle_bf16_to_f32(norm[h]) * scale)"),
+    "quant_uses_scale_not_inverse": ("oracle_bf16_to_f32(norm[h]) * inv)", "oracle_bf16_to_f32(norm[h]) * scale)"),
+    "quant_inverse_off": ("448.0f / amax : 1.0f", "440.0f / amax : 1.0f"),
     "quant_amax_signed": ("float v = fabsf(oracle_bf16_to_f32(norm[h]));", "float v = oracle_bf16_to_f32(norm[h]);"),
     "widen_drops_low_bit": (
         "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)(b & 0xFFFEu)) << 16;"),
