@@ -54,8 +54,10 @@ namespace {
 
 typedef void (*VecKernel)(const farn::Params);
 
-// Chunks in flight per thread that the stage kernels are built for.
-constexpr int kStageDepths[3] = {16, 12, 8};
+// Chunks in flight per thread that the stage kernels are built for (the
+// FP8-output kernels also at 6, so that two of their CTAs share an SM at
+// H = 8192).
+constexpr int kStageDepths[4] = {16, 12, 8, 6};
 
 template <bool Q>
 VecKernel pick_stage_q(int vpt, int r) {
@@ -63,10 +65,12 @@ VecKernel pick_stage_q(int vpt, int r) {
     if (r == 8) return &farn::farn_stage_kernel<2, 8, Q>;
     if (r == 12) return &farn::farn_stage_kernel<2, 12, Q>;
     if (r == 16) return &farn::farn_stage_kernel<2, 16, Q>;
+    if (Q && r == 6) return &farn::farn_stage_kernel<2, 6, true>;
   } else if (vpt == 4) {
     if (r == 8) return &farn::farn_stage_kernel<4, 8, Q>;
     if (r == 12) return &farn::farn_stage_kernel<4, 12, Q>;
     if (r == 16) return &farn::farn_stage_kernel<4, 16, Q>;
+    if (Q && r == 6) return &farn::farn_stage_kernel<4, 6, true>;
   }
   return nullptr;
 }
@@ -210,12 +214,12 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
   if ((int64_t)regs * nt * ctas > 65536) return false;
   const size_t budget = (size_t)ctx->max_smem / (size_t)ctas - 1024;
   int r = 0;
-  for (int i = 0; i < 3 && !r; ++i) {
+  for (int i = 0; i < (quant ? 4 : 3) && !r; ++i) {
     const int cand = kStageDepths[i];
     if (ctx->stage_r > 0 && cand != ctx->stage_r) continue;
     if ((size_t)cand * vpt * nt * 16 <= budget) r = cand;
   }
-  if (!r || !pick_stage(vpt, r)) return false;
+  if (!r || !pick_stage(vpt, r, quant)) return false;
   pl->variant = kVariantStage;
   pl->pb = 2;
   pl->cs = 1;
@@ -483,10 +487,11 @@ int farn_create(farn_ctx** out, int device) {
   }
   memset(c->stage_regs, 0, sizeof c->stage_regs);
   for (int vpt = 2; vpt <= 4; vpt *= 2) {
-    for (int i = 0; i < 6; ++i) {
-      // dynamic + static shared memory may not exceed the opt-in limit
+    for (int i = 0; i < 7; ++i) {
+      // dynamic + static shared memory may not exceed the opt-in limit;
+      // i < 3: plain kernels, i >= 3: FP8-output kernels (depths 16..6)
       cudaFuncAttributes fa;
-      const void* k = (const void*)pick_stage(vpt, kStageDepths[i % 3], i >= 3);
+      const void* k = (const void*)pick_stage(vpt, kStageDepths[i < 3 ? i : i - 3], i >= 3);
       if (cudaFuncGetAttributes(&fa, k) != cudaSuccess ||
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {

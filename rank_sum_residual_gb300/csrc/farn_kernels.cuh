@@ -831,6 +831,31 @@ farn_stage_kernel(const __grid_constant__ Params p) {
   int q = 0;     // chunk being consumed
   int it = 0;
   int res_slot = 0;
+  // FP8 output, pipelined: row i's amax is published at row i+1's
+  // sum-of-squares barrier, so each row costs one barrier; the last row's
+  // is published after the loop.
+  uint4 nb_prev[VPT];
+  float mx_prev = 0.0f;
+  int64_t row_prev = -1;
+  auto quant_store = [&](int64_t qrow, const float amax) {
+    const float scale = e4m3_row_scale(amax);
+    const float inv = e4m3_row_inv(amax);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) {
+        const uint32_t n[4] = {nb_prev[k].x, nb_prev[k].y, nb_prev[k].z, nb_prev[k].w};
+        uint32_t q8[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          q8[e] = pack_e4m3x2(bf_lo(n[e]) * inv, bf_hi(n[e]) * inv);
+        asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};"
+                     :: "l"(p.q_out + (qrow * hv + j) * 8), "r"(q8[0] | (q8[1] << 16)),
+                        "r"(q8[2] | (q8[3] << 16)) : "memory");
+      }
+    }
+    if (tid == 0) p.scale_out[qrow] = scale;
+  };
   for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
     const int64_t base = row * hv;
     float acc[VPT][8];
@@ -892,9 +917,23 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     ss = warp_sum(ss);
     float* ws = warp_ss[it & 1];
     if (lane == 0) ws[warp] = ss;
+    if constexpr (QUANT) {
+      if (row_prev >= 0) {
+        const float m = warp_max(mx_prev);
+        if (lane == 0) warp_mx[(it - 1) & 1][warp] = m;
+      }
+    }
     __syncthreads();
     float tot = 0.0f;
     for (int w = 0; w < nwarps; ++w) tot += ws[w];
+    if constexpr (QUANT) {
+      if (row_prev >= 0) {
+        const float* wm = warp_mx[(it - 1) & 1];
+        float amax = 0.0f;
+        for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, wm[w]);
+        quant_store(row_prev, amax);
+      }
+    }
     const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
     uint4 nb[VPT];
     float mx = 0.0f;
@@ -919,30 +958,23 @@ farn_stage_kernel(const __grid_constant__ Params p) {
       }
     }
     if constexpr (QUANT) {
-      // the row's amax (exact, NaN ignored), then E4M3(norm * 448 / amax)
-      mx = warp_max(mx);
-      float* wm = warp_mx[it & 1];
-      if (lane == 0) wm[warp] = mx;
+      // the row's amax (exact, NaN ignored) is reduced at the next row's
+      // barrier, or after the loop for the last row
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) nb_prev[k] = nb[k];
+      mx_prev = mx;
+      row_prev = row;
+    }
+  }
+  if constexpr (QUANT) {
+    if (row_prev >= 0) {
+      const float m = warp_max(mx_prev);
+      if (lane == 0) warp_mx[(it - 1) & 1][warp] = m;
       __syncthreads();
+      const float* wm = warp_mx[(it - 1) & 1];
       float amax = 0.0f;
       for (int w = 0; w < nwarps; ++w) amax = fmaxf(amax, wm[w]);
-      const float scale = e4m3_row_scale(amax);
-      const float inv = e4m3_row_inv(amax);
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int j = tid + k * nt;
-        if (j < hv) {
-          const uint32_t n[4] = {nb[k].x, nb[k].y, nb[k].z, nb[k].w};
-          uint32_t q8[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            q8[e] = pack_e4m3x2(bf_lo(n[e]) * inv, bf_hi(n[e]) * inv);
-          asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};"
-                       :: "l"(p.q_out + (base + j) * 8), "r"(q8[0] | (q8[1] << 16)),
-                          "r"(q8[2] | (q8[3] << 16)) : "memory");
-        }
-      }
-      if (tid == 0) p.scale_out[row] = scale;
+      quant_store(row_prev, amax);
     }
   }
   cp_async_wait<0>();   // nothing may land after the CTA exits
