@@ -436,16 +436,28 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The K steps run back to back; events between consecutive chunks of
+    # them (recorded on the same stream, no gap added) give the spread.
+    n_chunks = max(1, min(20, K // max(1, n_sets)))
+    bounds = [round(K * i / n_chunks) for i in range(n_chunks + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
     t_wall0 = time.time()
-    ev0.record(stream)
-    run_steps(K)
-    ev1.record(stream)
+    evs[0].record(stream)
+    for i in range(n_chunks):
+        run_steps(bounds[i + 1] - bounds[i])
+        evs[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dev)
+    chunk_ms = sorted(evs[i].elapsed_time(evs[i + 1]) / (bounds[i + 1] - bounds[i])
+                      for i in range(n_chunks) if bounds[i + 1] > bounds[i])
+
+    def pct(q):
+        return chunk_ms[min(len(chunk_ms) - 1, int(q * (len(chunk_ms) - 1) + 0.5))]
+    step_stats = {"chunks": len(chunk_ms), "p10_ms": pct(0.1), "median_ms": pct(0.5),
+                  "p90_ms": pct(0.9), "mean_ms": ms / K}
 
     # ---- per-call kernel time, right after the timed steps and under the
     # same clock sampling: each call alone, back to back over the input
@@ -506,6 +518,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "rows_per_s": rows_per_s,
             "pct_hbm_peak": 100.0 * value / world / peak,
+            "step_ms_spread": step_stats,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

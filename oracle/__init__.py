@@ -82,6 +82,15 @@ def _declare(lib):
     lib.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
     lib.oracle_quant_e4m3_row.argtypes = [u16p, ctypes.c_int64, u8p]
     lib.oracle_quant_e4m3_row.restype = ctypes.c_float
+    lib.oracle_moe_combine.argtypes = [u16p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_float), ctypes.c_int, u16p,
+                                       u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                                       u16p, u16p, u16p]
+    lib.oracle_moe_combine.restype = ctypes.c_int
+    lib.oracle_moe_combine_acc.argtypes = [u16p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                           ctypes.c_int64, ctypes.c_int64]
+    lib.oracle_moe_combine_acc.restype = ctypes.c_float
     return lib
 
 
@@ -211,6 +220,38 @@ def _Oracle_e4m3_to_f32(self, b: int) -> float:
     return float(self.lib.oracle_e4m3_to_f32(int(b)))
 
 
+def _Oracle_moe_combine(self, expert_out, index, gates, residual, weight, eps: float):
+    """MoE combine + residual + RMSNorm: expert_out uint16 [S,H], index
+    int32 [T,K], gates float32 [T,K], residual uint16 [T,H], weight [H]."""
+    expert_out = _u16(expert_out)
+    index = np.ascontiguousarray(index, dtype=np.int32)
+    gates = np.ascontiguousarray(gates, dtype=np.float32)
+    residual, weight = _u16(residual), _u16(weight)
+    T, H = residual.shape
+    S = expert_out.shape[0] if expert_out.size else 0
+    K = index.shape[1]
+    outs = [np.empty((T, H), np.uint16) for _ in range(3)]
+    rc = self.lib.oracle_moe_combine(
+        _p(expert_out), S, index.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        _pf(gates), K, _p(residual), _p(weight), eps, T, H, *[_p(o) for o in outs])
+    if rc != 0:
+        raise ValueError(f"oracle_moe_combine rejected its arguments (rc={rc})")
+    return tuple(outs)
+
+
+def _Oracle_moe_combine_acc(self, expert_out, index_row, gates_row, h: int) -> float:
+    """The fp32 accumulator of one element before its bf16 rounding."""
+    expert_out = _u16(expert_out)
+    index_row = np.ascontiguousarray(index_row, dtype=np.int32)
+    gates_row = np.ascontiguousarray(gates_row, dtype=np.float32)
+    S, H = expert_out.shape
+    return float(self.lib.oracle_moe_combine_acc(
+        _p(expert_out), S, index_row.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+        _pf(gates_row), index_row.size, H, h))
+
+
+Oracle.moe_combine = _Oracle_moe_combine
+Oracle.moe_combine_acc = _Oracle_moe_combine_acc
 Oracle.quant_e4m3 = _Oracle_quant
 Oracle.f32_to_e4m3 = _Oracle_e4m3
 Oracle.e4m3_to_f32 = _Oracle_e4m3_to_f32

@@ -278,3 +278,53 @@ float oracle_quant_e4m3_row(const uint16_t *norm, int64_t H, uint8_t *q)
     return scale;
 }
 
+/* ---------------------------------------------------------------------
+ * MoE combine ("local y reduce": the per-token weighted sum of its top-k
+ * expert outputs) fused with the same residual add + RMSNorm.  The page
+ * names the step but defines neither its weights nor its layout; reading:
+ *   expert_out  bf16 [n_slots, H], one row per (token, expert) assignment
+ *   index       int32 [T, K], the row of expert_out of token t's k-th
+ *               expert; -1 (or any value outside [0, n_slots)) is skipped
+ *   gates       fp32 [T, K], the routing weights
+ *   reduced[t,h] = bf16(acc), acc = -0; for k in 0..K-1, not skipped:
+ *                 acc = acc + (gates[t,k] * f(expert_out[index[t,k], h]))
+ *   with the product and the sum each rounded to fp32 (no fused
+ *   multiply-add), in k order; then residual_out and norm_out as in
+ *   oracle_forward.
+ * ------------------------------------------------------------------- */
+/* The fp32 accumulator of one element (token row `index_row`/`gates_row`,
+ * column h), before its rounding to bf16. */
+float oracle_moe_combine_acc(const uint16_t *expert_out, int64_t n_slots,
+                             const int32_t *index_row, const float *gates_row, int K,
+                             int64_t H, int64_t h)
+{
+    float acc = -0.0f;
+    for (int k = 0; k < K; ++k) {
+        int32_t s = index_row[k];
+        if (s < 0 || (int64_t)s >= n_slots)
+            continue;
+        float prod = gates_row[k] * oracle_bf16_to_f32(expert_out[(int64_t)s * H + h]);
+        acc = acc + prod;
+    }
+    return acc;
+}
+
+int oracle_moe_combine(const uint16_t *expert_out, int64_t n_slots, const int32_t *index,
+                       const float *gates, int K, const uint16_t *residual,
+                       const uint16_t *weight, float eps, int64_t T, int64_t H,
+                       uint16_t *reduced, uint16_t *residual_out, uint16_t *norm_out)
+{
+    if (K < 1 || T < 0 || H < 1 || n_slots < 0 || !index || !gates || !residual ||
+        !weight || !reduced || !residual_out || !norm_out || (n_slots > 0 && !expert_out))
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t off = t * H;
+        for (int64_t h = 0; h < H; ++h)
+            reduced[off + h] = oracle_f32_to_bf16(oracle_moe_combine_acc(
+                expert_out, n_slots, index + t * K, gates + t * K, K, H, h));
+        oracle_residual_add(reduced + off, residual + off, H, residual_out + off);
+        oracle_rmsnorm_row(residual_out + off, weight, eps, H, norm_out + off);
+    }
+    return 0;
+}
+

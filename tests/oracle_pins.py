@@ -504,4 +504,90 @@ def pin_quant_row_vs_exact_rounding(O):
             assert int(q[t][h]) == e4m3_exact(Fraction(float(d)) if d != 0 else float(d))
 
 
+# ---------------------------------------------------------------- MoE combine
+def _f32(q: Fraction) -> Fraction:
+    """Exact rational rounded to the nearest fp32 (ties to even)."""
+    return Fraction(float(np.float32(float(q)))) if q != 0 else Fraction(0)
+
+
+def pin_moe_combine_hand_case(O):
+    """Two tokens, K = 3: gates 0.5 / 0.25 / 2, one slot skipped (-1), one
+    out of range (7 >= 4 slots)."""
+    one = bx.bits(1)
+    ex = np.array([[bx.bits(4), bx.bits(1)], [bx.bits(8), bx.bits(-2)],
+                   [bx.bits(0.5), bx.bits(3)], [bx.bits(-1), bx.bits(0)]], np.uint16)
+    idx = np.array([[0, 1, -1], [2, 7, 3]], np.int32)
+    g = np.array([[0.5, 0.25, 9.0], [2.0, 5.0, 1.0]], np.float32)
+    res = np.zeros((2, 2), np.uint16)
+    red, ro, _ = O.moe_combine(ex, idx, g, res, np.array([one, one], np.uint16), 1e-6)
+    # token 0: 0.5*4 + 0.25*8 = 4, 0.5*1 + 0.25*(-2) = 0; token 1: 2*0.5 - 1 = 0, 2*3 + 0 = 6
+    assert [bx.decode(int(v)) for v in red[0]] == [4, 0]
+    assert [bx.decode(int(v)) for v in red[1]] == [0, 6]
+
+
+def pin_moe_combine_unit_gates_is_rank_sum(O):
+    """With every gate 1 and index[t,k] = the row of partial k, the combine
+    is exactly the rank sum of the partials (same fp32 order and roundings,
+    1 * x being exact)."""
+    rng = np.random.default_rng(47)
+    T, H, K = 6, 40, 5
+    xs = [(rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+          for _ in range(K)]
+    res = (rng.normal(size=(T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = (rng.normal(1, .1, H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    ex = np.concatenate(xs, axis=0)                       # slot k*T + t
+    idx = np.array([[k * T + t for k in range(K)] for t in range(T)], np.int32)
+    a = O.moe_combine(ex, idx, np.ones((T, K), np.float32), res, w, 1e-6)
+    b = O.forward(xs, res, w, 1e-6)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def pin_moe_combine_fp32_accumulator(O):
+    """The fp32 accumulator itself against exact rationals rounded to fp32
+    after every product and every sum (a fused multiply-add, a reordering or
+    a dropped term changes it)."""
+    rng = np.random.default_rng(59)
+    S, H, K = 16, 32, 7
+    ex = (rng.normal(size=(S, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for trial in range(12):
+        idx = rng.integers(-1, S + 1, size=K).astype(np.int32)
+        g = rng.uniform(0, 1, size=K).astype(np.float32)
+        for h in range(H):
+            acc = Fraction(0)
+            for k in range(K):
+                s_ = int(idx[k])
+                if 0 <= s_ < S:
+                    acc = _f32(acc + _f32(Fraction(float(g[k])) * bx.decode(int(ex[s_, h]))))
+            got = O.moe_combine_acc(ex, idx, g, h)
+            assert Fraction(got) == acc, (trial, h, got, float(acc))
+
+
+def pin_moe_combine_exact_rounding(O):
+    """Against exact rationals with each product and each sum rounded to
+    fp32 in k order (no fused multiply-add): bit for bit."""
+    rng = np.random.default_rng(53)
+    T, H, K, S = 4, 24, 6, 20
+    ex = (rng.normal(size=(S, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    idx = rng.integers(-1, S + 2, size=(T, K)).astype(np.int32)
+    g = rng.uniform(0, 1, size=(T, K)).astype(np.float32)
+    res = np.zeros((T, H), np.uint16)
+    red, _, _ = O.moe_combine(ex, idx, g, res, np.full(H, bx.bits(1), np.uint16), 1e-6)
+    for t in range(T):
+        for h in range(H):
+            acc, any_term = Fraction(0), False
+            for k in range(K):
+                s_ = int(idx[t, k])
+                if s_ < 0 or s_ >= S:
+                    continue
+                prod = _f32(Fraction(float(g[t, k])) * bx.decode(int(ex[s_, h])))
+                acc = _f32(acc + prod)
+                any_term = True
+            got = int(red[t, h])
+            if acc == 0:
+                assert (got & 0x7FFF) == 0
+            else:
+                assert got == bx.round_rne(acc), (t, h, hex(got), hex(bx.round_rne(acc)))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -69,6 +69,12 @@ MUTANTS = {
     "quant_uses_scale_not_inverse": ("oracle_bf16_to_f32(norm[h]) * inv)", "oracle_bf16_to_f32(norm[h]) * scale)"),
     "quant_inverse_off": ("448.0f / amax : 1.0f", "440.0f / amax : 1.0f"),
     "quant_amax_signed": ("float v = fabsf(oracle_bf16_to_f32(norm[h]));", "float v = oracle_bf16_to_f32(norm[h]);"),
+    "combine_fused_multiply_add": (
+        "        acc = acc + prod;",
+        "        acc = fmaf(gates_row[k], oracle_bf16_to_f32(expert_out[(int64_t)s * H + h]), acc);"),
+    "combine_gate_index_wrong": ("gates_row[k] * oracle", "gates_row[0] * oracle"),
+    "combine_no_range_check": ("if (s < 0 || (int64_t)s >= n_slots)", "if (s < 0)"),
+    "combine_slot_row_wrong": ("expert_out[(int64_t)s * H + h]", "expert_out[(int64_t)s + h]"),
     "widen_drops_low_bit": (
         "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)(b & 0xFFFEu)) << 16;"),
 }
