@@ -58,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm",
-                             "prefill_f32", "prefill_fp8"])
+                             "prefill_f32", "prefill_fp8", "moe_combine"])
     ap.add_argument("--in-place", action="store_true",
                     help="write residual_out over the residual (in-place residual update)")
     ap.add_argument("--impl", default="farn", choices=["farn", "reference"])
@@ -225,7 +225,10 @@ def time_oracle_rows(sample, rows_total_target=None, seconds=10.0):
     t0 = time.perf_counter()
     while True:
         for p, xs, res, w in sample:
-            outs = O.forward(xs, res, w, p.eps)
+            if p.kind == "moe_combine":
+                outs = O.moe_combine(*xs, res, w, p.eps)
+            else:
+                outs = O.forward(xs, res, w, p.eps)
             if p.fp8_out:
                 O.quant_e4m3(outs[2])
             r = res.shape[0]
@@ -271,7 +274,11 @@ def run_reference(args):
         for _ in range(rows_per_step):
             p, xs, res, w, t = flat[cursor % len(flat)]
             cursor += 1
-            outs = O.forward([x[t:t + 1] for x in xs], res[t:t + 1], w, p.eps)
+            if p.kind == "moe_combine":
+                ex, index, gates = xs
+                outs = O.moe_combine(ex, index[t:t + 1], gates[t:t + 1], res[t:t + 1], w, p.eps)
+            else:
+                outs = O.forward([x[t:t + 1] for x in xs], res[t:t + 1], w, p.eps)
             if p.fp8_out:
                 O.quant_e4m3(outs[2])
             b += call_bytes(p, 1)
@@ -475,6 +482,9 @@ def run_gpu(args):
     for j, c in enumerate(per_call):
         c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
         c["frac"] = c["gbs"] / peak
+        if problems[j].kind == "moe_combine":
+            c["variant"] = "combine (one CTA per row, gathered rows)"
+            continue
         v, cs, thr = farn.farn_plan_typed(ctx.handle, *plan_args(sets[0][j]))
         c["variant"] = f"{v} cluster={cs} threads={thr}"
     dom = max(per_call, key=lambda c: c["kernel_us"] * c["count_per_step"])
@@ -535,7 +545,7 @@ def run_gpu(args):
 
 KERNELS = {"row": "farn_vec_kernel", "cluster": "farn_vec_kernel",
            "generic": "farn_generic_kernel", "bulk": "farn_bulk_kernel",
-           "stage": "farn_stage_kernel"}
+           "stage": "farn_stage_kernel", "combine": "farn_combine_kernel"}
 KERNEL_SOURCES = ("rank_sum_residual_gb300/csrc/farn_kernels.cuh",)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
@@ -600,6 +610,10 @@ def make_outputs(p, dev):
 def call_forward(p, xs, res, w, outs, ctx, stream):
     """One operator call through the binding of the C ABI."""
     import rank_sum_residual_gb300 as farn
+    if p.kind == "moe_combine":
+        ex, index, gates = xs
+        farn.moe_combine(ex, index, gates, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
+        return
     if not p.fp8_out:
         farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
         return
@@ -625,12 +639,19 @@ def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
     out = []
     for p in problems:
         copies = max(2, math.ceil(2 * l2_bytes / p.algorithmic_bytes()))
-        xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
-        xs = [torch.empty((copies, p.T, p.H), dtype=xdt, device=dev) for _ in range(p.W)]
         res = torch.empty((copies, p.T, p.H), dtype=torch.bfloat16, device=dev)
         w = torch.empty((p.H,), dtype=torch.bfloat16, device=dev)
-        for r, x in enumerate(xs):
-            synth.fill_device(x, p.seed + 1, r, p.x)
+        if p.kind == "moe_combine":
+            ex = torch.empty((copies, p.T * p.W, p.H), dtype=torch.bfloat16, device=dev)
+            synth.fill_device(ex, p.seed + 1, 0, p.x)
+            index, gates = (torch.from_numpy(a).to(dev) for a in synth.moe_routing(p))
+            ins = [(ex[c], index, gates) for c in range(copies)]
+        else:
+            xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
+            xs = [torch.empty((copies, p.T, p.H), dtype=xdt, device=dev) for _ in range(p.W)]
+            for r, x in enumerate(xs):
+                synth.fill_device(x, p.seed + 1, r, p.x)
+            ins = [[x[c] for x in xs] for c in range(copies)]
         synth.fill_device(res, p.seed + 1, synth.STREAM_RESIDUAL, p.residual)
         synth.fill_device(w, p.seed + 1, synth.STREAM_WEIGHT, p.weight)
         outs = [make_outputs(p, dev) for _ in range(copies)]
@@ -639,7 +660,7 @@ def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
         with torch.cuda.graph(g):
             for i in range(reps):
                 c = i % copies
-                call_forward(p, [x[c] for x in xs], res[c], w, outs[c], ctx, None)
+                call_forward(p, ins[c], res[c], w, outs[c], ctx, None)
         g.replay()
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -651,7 +672,7 @@ def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
         out.append(dict(call=p.name, T=p.T, W=p.W, H=p.H, bytes=p.algorithmic_bytes(),
                         count_per_step=1, launches_timed=3 * reps, rotating_copies=copies,
                         kernel_us=e0.elapsed_time(e1) / (3 * reps) * 1e3))
-        del g, xs, res, w, outs
+        del g, ins, res, w, outs
         torch.cuda.empty_cache()
     return out
 
@@ -669,14 +690,13 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
     import rank_sum_residual_gb300 as farn
 
     # inputs and outputs packed as bytes (fp32 partials, E4M3 outputs)
-    in_bytes = sum(p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
-                   for p in problems)
+    in_bytes = sum(p.read_bytes() for p in problems)
     out_bytes = sum(p.write_bytes() for p in problems)
     host_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
     host_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
     off = 0
     for p, xs, res, w, outs in calls:          # the step's inputs, packed
-        for t in (*xs, res, w):
+        for t in (*xs, res, w):                # (expert_out, index, gates) for MoE
             b = t.reshape(-1).view(torch.uint8)
             host_in[off:off + b.numel()].copy_(b)
             off += b.numel()
@@ -692,8 +712,14 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
             return t
         for p in problems:
             n = p.T * p.H
-            xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
-            xs = [take(dev_in, "in", n * p.partial_bytes, xdt, (p.T, p.H)) for _ in range(p.W)]
+            if p.kind == "moe_combine":
+                xs = (take(dev_in, "in", n * p.W * 2, torch.bfloat16, (p.T * p.W, p.H)),
+                      take(dev_in, "in", p.T * p.W * 4, torch.int32, (p.T, p.W)),
+                      take(dev_in, "in", p.T * p.W * 4, torch.float32, (p.T, p.W)))
+            else:
+                xdt = torch.float32 if p.partial_bytes == 4 else torch.bfloat16
+                xs = [take(dev_in, "in", n * p.partial_bytes, xdt, (p.T, p.H))
+                      for _ in range(p.W)]
             res = take(dev_in, "in", n * 2, torch.bfloat16, (p.T, p.H))
             w = take(dev_in, "in", p.H * 2, torch.bfloat16, (p.H,))
             outs = [take(dev_out, "out", n * 2, torch.bfloat16, (p.T, p.H)) for _ in range(2)]

@@ -222,6 +222,29 @@ int farn_forward_quant(const farn_ctx *ctx,
                        void *norm_q, float *row_scale,
                        cudaStream_t stream);
 
+/* farn_moe_combine - the MoE "local y reduce" fused with the same
+ * residual add + RMSNorm.  (The page names the per-token reduction of
+ * expert outputs but defines neither its weights nor its layout; this is
+ * the plain reading.)  For each token t and column h:
+ *     reduced[t,h] = bf16(acc),  acc = -0; for k = 0..K-1, slot s = index[t*K+k]
+ *                    in [0, n_slots):  acc = acc + gates[t*K+k] * f(expert_out[s,h])
+ * with the product and the sum each rounded to fp32 (no fused multiply-add),
+ * k in order; slots outside [0, n_slots) (e.g. -1 for a dropped expert) are
+ * skipped, and are never read.  residual_out and norm_out then follow as in
+ * farn_forward.
+ *   expert_out  bf16 [n_slots, H], one row per (token, expert) assignment
+ *   index       int32 [T, K] (4-byte aligned), gates fp32 [T, K] (4-byte aligned)
+ *   K           1 .. FARN_MAX_W
+ * Other arguments, layouts, ownership, in-place residual_out and errors as
+ * for farn_forward; outputs may not overlap expert_out, index or gates. */
+int farn_moe_combine(const farn_ctx *ctx,
+                     const void *expert_out, int64_t n_slots,
+                     const int32_t *index, const float *gates, int K,
+                     const void *residual, const void *weight, float eps,
+                     int64_t T, int64_t H,
+                     void *reduced_out, void *residual_out, void *norm_out,
+                     cudaStream_t stream);
+
 /* Flags of farn_plan_typed. */
 #define FARN_PLAN_FP8_OUT 1   /* the call also writes the FP8 norm output */
 

@@ -25,6 +25,7 @@ __all__ = [
     "farn_create", "farn_destroy", "farn_forward", "farn_check_args",
     "farn_plan", "farn_status_string", "farn_device_status", "farn_forward_noalloc",
     "farn_forward_typed", "farn_plan_typed", "farn_forward_quant", "forward_quant",
+    "farn_moe_combine", "moe_combine",
     "FARN_BF16", "FARN_F32",
     "forward", "VARIANTS",
 ]
@@ -70,6 +71,9 @@ def _load():
         lib.farn_forward_quant.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64,
                                            vp, vp, vp, vp, vp, vp]
         lib.farn_forward_quant.restype = i32
+        lib.farn_moe_combine.argtypes = [vp, cvp, i64, cvp, cvp, i32, cvp, cvp, f32, i64, i64,
+                                         vp, vp, vp, vp]
+        lib.farn_moe_combine.restype = i32
         lib.farn_check_args.argtypes = [pvp, i32, cvp, cvp, f32, i64, i64,
                                         cvp, cvp, cvp]
         lib.farn_check_args.restype = i32
@@ -154,6 +158,46 @@ def farn_forward_quant(ctx, partials, partial_dtype, W, residual, weight, eps, T
         ctypes.c_void_p(int(norm_out)) if norm_out else None,
         ctypes.c_void_p(int(norm_q)), ctypes.c_void_p(int(row_scale)),
         ctypes.c_void_p(int(stream)))
+
+
+def farn_moe_combine(ctx, expert_out, n_slots, index, gates, K, residual, weight, eps, T, H,
+                     reduced_out, residual_out, norm_out, stream=0) -> int:
+    """C ``farn_moe_combine`` on raw device addresses (ints)."""
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    return _load().farn_moe_combine(
+        ctypes.c_void_p(ctx) if ctx else None, v(expert_out), int(n_slots), v(index), v(gates),
+        int(K), v(residual), v(weight), float(eps), int(T), int(H), v(reduced_out),
+        v(residual_out), v(norm_out), ctypes.c_void_p(int(stream)))
+
+
+def moe_combine(expert_out, index, gates, residual, weight, eps: float, out=None, ctx=None,
+                stream=None):
+    """MoE combine + residual + RMSNorm on torch CUDA tensors: expert_out bf16
+    [S,H], index int32 [T,K], gates fp32 [T,K], residual bf16 [T,H], weight
+    bf16 [H].  Returns (reduced, residual_out, norm_out)."""
+    import torch
+    T, H = residual.shape
+    dev = residual.device
+    S = expert_out.shape[0]
+    _check_tensor(expert_out, "expert_out", (S, H), dev)
+    K = index.shape[1] if index.dim() == 2 else -1
+    _check_tensor(index, "index", (T, K), dev, (torch.int32,))
+    _check_tensor(gates, "gates", (T, K), dev, (torch.float32,))
+    _check_tensor(residual, "residual", (T, H), dev)
+    _check_tensor(weight, "weight", (H,), dev)
+    if out is None:
+        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
+        _check_tensor(t, name, (T, H), dev)
+    c = ctx if ctx is not None else _context_for(dev.index)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = farn_moe_combine(c.handle, expert_out.data_ptr(), S, index.data_ptr(), gates.data_ptr(),
+                          K, residual.data_ptr(), weight.data_ptr(), eps, T, H,
+                          out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
+                          s.cuda_stream)
+    if st != FARN_OK:
+        raise FarnError(st, "farn_moe_combine")
+    return out
 
 
 def farn_forward_noalloc(device, partials, W, residual, weight, eps, T, H,

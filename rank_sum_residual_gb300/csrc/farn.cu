@@ -45,7 +45,8 @@ struct farn_ctx {
   int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
   int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
   int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
-  int stage_regs[2][2];  // registers per thread of the stage kernels [FP8 output][4 vectors]
+  int stage_regs[3][2];  // registers per thread of the staged kernels
+                         // [plain, FP8 output, MoE combine][4 vectors]
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
 };
@@ -78,6 +79,19 @@ VecKernel pick_stage_q(int vpt, int r) {
 // quant: the instantiation that also writes the FP8 output
 VecKernel pick_stage(int vpt, int r, bool quant = false) {
   return quant ? pick_stage_q<true>(vpt, r) : pick_stage_q<false>(vpt, r);
+}
+
+VecKernel pick_combine_stage(int vpt, int r) {
+  if (vpt == 2) {
+    if (r == 8) return &farn::farn_combine_stage_kernel<2, 8>;
+    if (r == 12) return &farn::farn_combine_stage_kernel<2, 12>;
+    if (r == 16) return &farn::farn_combine_stage_kernel<2, 16>;
+  } else if (vpt == 4) {
+    if (r == 8) return &farn::farn_combine_stage_kernel<4, 8>;
+    if (r == 12) return &farn::farn_combine_stage_kernel<4, 12>;
+    if (r == 16) return &farn::farn_combine_stage_kernel<4, 16>;
+  }
+  return nullptr;
 }
 
 VecKernel pick_generic(int pb) {
@@ -204,13 +218,15 @@ int choose_vpt(int64_t sv) {
 //      that give >= 320 threads per SM and fit registers and shared memory;
 //   2. else one CTA per SM, 2 then 4 vectors per thread;
 // each with the largest of 16 / 12 / 8 chunks in flight per thread that fits.
+// kind: 0 plain stage kernel, 1 with the FP8 output, 2 the staged MoE combine
 bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T,
-               bool quant) {
+               int kind) {
+  const bool quant = kind == 1;
   if (ctx->force_vpt > 0 && ctx->force_vpt != vpt) return false;
   if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
   const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
   if (nt > 512) return false;
-  const int regs = ctx->stage_regs[quant][vpt >= 4];
+  const int regs = ctx->stage_regs[kind][vpt >= 4];
   if ((int64_t)regs * nt * ctas > 65536) return false;
   const size_t budget = (size_t)ctx->max_smem / (size_t)ctas - 1024;
   int r = 0;
@@ -219,7 +235,8 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
     if (ctx->stage_r > 0 && cand != ctx->stage_r) continue;
     if ((size_t)cand * vpt * nt * 16 <= budget) r = cand;
   }
-  if (!r || !pick_stage(vpt, r, quant)) return false;
+  if (!r || !(kind == 2 ? pick_combine_stage(vpt, r) : pick_stage(vpt, r, quant)))
+    return false;
   pl->variant = kVariantStage;
   pl->pb = 2;
   pl->cs = 1;
@@ -233,21 +250,21 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
 }
 
 // bf16 partials only (fp32 partials take the row kernel, see the kernel).
-bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, bool quant) {
+bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int kind) {
   const int64_t hv = H / 8;
   const int vpts[2] = {4, 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
-    return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, quant) ||
-           stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T, quant);
+    return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, kind) ||
+           stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T, kind);
   for (int i = 0; i < 2; ++i) {
     const int vpt = vpts[i];
     const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
     int ctas = (int)((320 + nt - 1) / nt);
     if (ctas < 2) ctas = 2;
     for (; ctas <= 4; ++ctas)
-      if (stage_fit(ctx, hv, vpt, ctas, pl, T, quant)) return true;
+      if (stage_fit(ctx, hv, vpt, ctas, pl, T, kind)) return true;
   }
-  return stage_fit(ctx, hv, 2, 1, pl, T, quant) || stage_fit(ctx, hv, 4, 1, pl, T, quant);
+  return stage_fit(ctx, hv, 2, 1, pl, T, kind) || stage_fit(ctx, hv, 4, 1, pl, T, kind);
 }
 
 int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
@@ -271,7 +288,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
                   ctx->force_cluster == 0)) &&
-      make_stage_plan(ctx, T, H, &pl, quant)) {
+      make_stage_plan(ctx, T, H, &pl, quant ? 1 : 0)) {
     *out = pl;
     return FARN_OK;
   }
@@ -502,6 +519,19 @@ int farn_create(farn_ctx** out, int device) {
       int& regs = c->stage_regs[i >= 3][vpt >= 4];
       if (fa.numRegs > regs) regs = fa.numRegs;
     }
+    for (int i = 0; i < 3; ++i) {       // the staged MoE combine
+      cudaFuncAttributes fa;
+      const void* k = (const void*)pick_combine_stage(vpt, kStageDepths[i]);
+      if (cudaFuncGetAttributes(&fa, k) != cudaSuccess ||
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {
+        delete c;
+        cudaGetLastError();
+        return FARN_ERR_CUDA;
+      }
+      int& regs = c->stage_regs[2][vpt >= 4];
+      if (fa.numRegs > regs) regs = fa.numRegs;
+    }
   }
   // The bulk kernel's status word: set on a bounded-wait timeout, read and
   // cleared by farn_device_status.
@@ -707,6 +737,102 @@ int farn_forward_quant(const farn_ctx* ctx, const void* const* partials, int par
                        void* norm_q, float* row_scale, cudaStream_t stream) {
   return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
                       reduced_out, residual_out, norm_out, norm_q, row_scale, true, stream);
+}
+
+// ------------------------------------------------------------------------
+// MoE combine + residual + RMSNorm.
+int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slots,
+                     const int32_t* index, const float* gates, int K, const void* residual,
+                     const void* weight, float eps, int64_t T, int64_t H, void* reduced_out,
+                     void* residual_out, void* norm_out, cudaStream_t stream) {
+  if (!ctx || K < 1 || K > FARN_MAX_W || T < 0 || H < 1 || n_slots < 0)
+    return FARN_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 4 || (T > 0 && T > INT64_MAX / (4 * H)) ||
+      (n_slots > 0 && n_slots > INT64_MAX / (2 * H)))
+    return FARN_ERR_INVALID_ARG;
+  if (T == 0) return FARN_OK;
+  if (!index || !gates || !residual || !weight || !reduced_out || !residual_out || !norm_out ||
+      (n_slots > 0 && !expert_out))
+    return FARN_ERR_INVALID_ARG;
+  if (((uintptr_t)index & 3u) || ((uintptr_t)gates & 3u)) return FARN_ERR_INVALID_ARG;
+  const int64_t nb = T * H * 2, eb = n_slots * H * 2, ib = T * K * 4, wb = H * 2;
+  const void* outs[3] = {reduced_out, residual_out, norm_out};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], nb, outs[j], nb)) return FARN_ERR_ALIAS;
+    if (overlaps(outs[i], nb, expert_out, eb) || overlaps(outs[i], nb, index, ib) ||
+        overlaps(outs[i], nb, gates, ib) || overlaps(outs[i], nb, weight, wb))
+      return FARN_ERR_ALIAS;
+    const bool inplace_residual = (i == 1 && residual_out == residual);
+    if (!inplace_residual && overlaps(outs[i], nb, residual, nb)) return FARN_ERR_ALIAS;
+  }
+  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
+    return FARN_ERR_CUDA;
+
+  // Kernel: one CTA per row, every thread one vector of each gathered row
+  // for few rows (all loads in flight at once), 4 vectors otherwise; the
+  // generic kernel for odd shapes and alignments.
+  const int64_t hv = H / 8;
+  const bool vec_ok = H % 8 == 0 && aligned16(residual) && aligned16(weight) &&
+                      aligned16(reduced_out) && aligned16(residual_out) &&
+                      aligned16(norm_out) && (n_slots == 0 || aligned16(expert_out));
+  int vpt = T < ctx->small_t ? (hv <= 512 ? 1 : (hv <= 1024 ? 2 : 4)) : choose_vpt(hv);
+  if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
+  int64_t threads = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
+  const bool generic = !vec_ok || threads > 512 || ctx->force_variant == kVariantGeneric;
+  if (generic) threads = 256;
+  // The staged gather kernel on request only: on GB300 it measured no
+  // faster than the row kernel for the combine (80.1 % vs 81.4 % of the
+  // copy bandwidth at T = 4096, K = 8, H = 7168).
+  Plan spl;
+  const bool staged = !generic && ctx->force_variant == kVariantStage &&
+                      make_stage_plan(ctx, T, H, &spl, 2);
+  if (ctx->force_variant == kVariantStage && !staged) return FARN_ERR_UNSUPPORTED;
+  farn::Params prm;
+  memset(&prm, 0, sizeof prm);
+  prm.residual = residual;
+  prm.weight = weight;
+  prm.reduced = reduced_out;
+  prm.residual_out = residual_out;
+  prm.norm_out = norm_out;
+  prm.T = T;
+  prm.H = H;
+  prm.W = K;
+  prm.eps = eps;
+  prm.expert_out = expert_out;
+  prm.index = index;
+  prm.gates = gates;
+  prm.n_slots = n_slots;
+
+  DeviceGuard g(ctx->device);
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  cudaLaunchConfig_t cfg = {};
+  const int64_t grid = staged ? spl.grid : (T < 0x7FFFFFFF ? T : 0x7FFFFFFF);
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)(staged ? spl.threads : threads), 1, 1);
+  cfg.dynamicSmemBytes = staged ? spl.smem : 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = ctx->pdl ? 1 : 0;
+  cudaError_t err;
+  if (generic) {
+    err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel<2, true>, prm);
+  } else if (staged) {
+    err = cudaLaunchKernelEx(&cfg, pick_combine_stage(spl.vpt, spl.stage_r), prm);
+  } else {
+    VecKernel k = vpt == 1 ? &farn::farn_combine_kernel<1>
+                           : (vpt == 2 ? &farn::farn_combine_kernel<2> : &farn::farn_combine_kernel<4>);
+    err = cudaLaunchKernelEx(&cfg, k, prm);
+  }
+  if (err != cudaSuccess) {
+    cudaGetLastError();
+    return FARN_ERR_CUDA;
+  }
+  return FARN_OK;
 }
 
 // ------------------------------------------------------------------------

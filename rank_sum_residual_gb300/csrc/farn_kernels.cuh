@@ -48,6 +48,12 @@ struct Params {
   // bytes and scale_out [T] fp32, or null; norm_out may then be null too
   uint8_t* q_out;
   float* scale_out;
+  // MoE combine only (farn_combine_kernel, farn_generic_kernel<2, true>):
+  // W is K, the experts per token
+  const void* expert_out;  // bf16 [n_slots, H]
+  const int32_t* index;    // [T, K]; -1 or out of [0, n_slots): skipped
+  const float* gates;      // [T, K]
+  int64_t n_slots;
   // bulk (TMA-staged) kernel only
   int* err;               // device status word, bits of kBulkErr* on a timeout
   uint32_t stages;        // shared-memory ring stages
@@ -402,7 +408,7 @@ farn_vec_kernel(const __grid_constant__ Params p) {
 // -------------------------------------------------------- generic kernel
 // Any H, any alignment: one CTA per row, scalar bf16 accesses, two passes
 // (the second re-reads the residual_out this same thread wrote).
-template <int PB = 2>
+template <int PB = 2, bool COMBINE = false>
 __global__ void __launch_bounds__(256)
 farn_generic_kernel(const __grid_constant__ Params p) {
   const int tid = threadIdx.x;
@@ -422,11 +428,23 @@ farn_generic_kernel(const __grid_constant__ Params p) {
     float ss = 0.0f;
     for (int64_t h = tid; h < p.H; h += blockDim.x) {
       float acc = -0.0f;
-      for (int r = 0; r < p.W; ++r) {
-        if (PB == 2)
-          acc += __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p.x[r])[off + h] << 16);
-        else
-          acc += reinterpret_cast<const float*>(p.x[r])[off + h];
+      if constexpr (COMBINE) {
+        // MoE combine: gates * gathered expert rows, product and sum each
+        // rounded (no fused multiply-add), k in order, bad slots skipped
+        const uint16_t* ex = reinterpret_cast<const uint16_t*>(p.expert_out);
+        for (int k = 0; k < p.W; ++k) {
+          const int32_t sl = p.index[row * p.W + k];
+          if (sl < 0 || (int64_t)sl >= p.n_slots) continue;
+          const float x = __uint_as_float((uint32_t)ex[(int64_t)sl * p.H + h] << 16);
+          acc = __fadd_rn(acc, __fmul_rn(p.gates[row * p.W + k], x));
+        }
+      } else {
+        for (int r = 0; r < p.W; ++r) {
+          if (PB == 2)
+            acc += __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(p.x[r])[off + h] << 16);
+          else
+            acc += reinterpret_cast<const float*>(p.x[r])[off + h];
+        }
       }
       const uint16_t rb = to_bf16(acc);
       red_out[off + h] = rb;
@@ -471,6 +489,135 @@ farn_generic_kernel(const __grid_constant__ Params p) {
         p.q_out[off + h] = (uint8_t)(pack_e4m3x2(n * inv, 0.0f) & 0xFFu);
       }
       if (tid == 0) p.scale_out[row] = scale;
+    }
+  }
+}
+
+// ------------------------------------------------------ MoE combine kernel
+// The per-token weighted sum of its K expert rows (the MoE "local y
+// reduce"), fused with the same residual add + RMSNorm epilogue as
+// farn_vec_kernel (one CTA per row).  Row t reads index[t,0..K) and
+// gates[t,0..K) (every thread the same K words: broadcast through L1), then
+// gathers 16-byte vectors of the selected rows of expert_out, G slots at a
+// time, and accumulates gate * x with the product and the sum each rounded
+// to fp32 (__fmul_rn / __fadd_rn: no fused multiply-add), k in order.
+// Slots outside [0, n_slots) are skipped, so a bad index never leads to an
+// out-of-bounds load.
+template <int VPT>
+__global__ void __launch_bounds__(512)
+farn_combine_kernel(const __grid_constant__ Params p) {
+  constexpr int G = (8 / VPT) > 0 ? (8 / VPT) : 1;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const int64_t hv = p.H >> 3;
+  const int sv = (int)hv;
+  const int K = p.W;
+  const float Hf = (float)p.H;
+  __shared__ float warp_ss[2][32];
+  const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight);
+  const uint4* __restrict__ ex4 = reinterpret_cast<const uint4*>(p.expert_out);
+
+  pdl_wait();
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+    const int64_t base = row * hv;
+    uint4 rv[VPT];
+    float acc[VPT][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) rv[k] = ld_coherent(reinterpret_cast<const uint4*>(p.residual) + base + j);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
+    }
+    for (int k0 = 0; k0 < K; k0 += G) {
+      uint4 xv[G][VPT];
+      float gt[G];
+      bool ok[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int k = k0 + g;
+        int32_t sl = -1;
+        gt[g] = 0.0f;
+        if (k < K) {
+          sl = __ldg(p.index + row * K + k);
+          gt[g] = __ldg(p.gates + row * K + k);
+        }
+        ok[g] = sl >= 0 && (int64_t)sl < p.n_slots;
+        const uint4* xp = ex4 + (ok[g] ? (int64_t)sl * hv : 0);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+          const int j = tid + v * blockDim.x;
+          xv[g][v] = make_uint4(0u, 0u, 0u, 0u);
+          if (ok[g] && j < sv) xv[g][v] = ld_stream(xp + j);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (ok[g]) {
+#pragma unroll
+          for (int v = 0; v < VPT; ++v) {
+            const uint32_t xw[4] = {xv[g][v].x, xv[g][v].y, xv[g][v].z, xv[g][v].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[v][2 * e] = __fadd_rn(acc[v][2 * e], __fmul_rn(gt[g], bf_lo(xw[e])));
+              acc[v][2 * e + 1] = __fadd_rn(acc[v][2 * e + 1], __fmul_rn(gt[g], bf_hi(xw[e])));
+            }
+          }
+        }
+      }
+    }
+    if (row + gridDim.x >= p.T) pdl_trigger();
+
+    uint4 ro[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) {
+        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        uint32_t red[4], out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
+          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+          out[e] = pack_bf16x2(s0, s1);
+          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+          ss = fmaf(q0, q0, ss);
+          ss = fmaf(q1, q1, ss);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                  make_uint4(red[0], red[1], red[2], red[3]));
+        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+      }
+    }
+    ss = warp_sum(ss);
+    float* ws = warp_ss[it & 1];
+    if (lane == 0) ws[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += ws[w];
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * blockDim.x;
+      if (j < sv) {
+        const uint4 wk = ld_keep(wv4 + j);
+        const uint32_t q[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
+        const uint32_t w[4] = {wk.x, wk.y, wk.z, wk.w};
+        uint32_t n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n0 = (bf_lo(q[e]) * rstd) * bf_lo(w[e]);
+          const float n1 = (bf_hi(q[e]) * rstd) * bf_hi(w[e]);
+          n[e] = pack_bf16x2(n0, n1);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                  make_uint4(n[0], n[1], n[2], n[3]));
+      }
     }
   }
 }
@@ -978,6 +1125,180 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     }
   }
   cp_async_wait<0>();   // nothing may land after the CTA exits
+}
+
+// ------------------------------------ staged MoE combine (cp.async gather)
+// The MoE combine for long inputs, staged like farn_stage_kernel: each
+// persistent CTA walks its rows; the chunks of a row are its K gathered
+// expert rows (expert_out[index[t,k]]) and then its residual row; every
+// thread keeps R chunks of its own 16-byte vectors in flight with
+// cp.async.  The issuing thread reads the slot index through L1 when it
+// issues a chunk (a skipped slot issues no copy, only an empty group); the
+// consumer reads the same index and the gate, and adds gate * x with the
+// product and the sum each rounded (no fused multiply-add), k in order.
+template <int VPT, int R>
+__global__ void __launch_bounds__(512)
+farn_combine_stage_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nwarps = (nt + 31) >> 5;
+  const int64_t hv = p.H >> 3;
+  const int K = p.W;
+  const float Hf = (float)p.H;
+  __shared__ float warp_ss[2][32];
+  const uint32_t slots = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint4* __restrict__ ex4 = reinterpret_cast<const uint4*>(p.expert_out);
+  auto slot_addr = [&](int s, int k) -> uint32_t {
+    return slots + (uint32_t)(((s * VPT + k) * nt + tid) * 16);
+  };
+  auto slot_of = [&](int64_t row, int c) -> int32_t {
+    const int32_t sl = __ldg(p.index + row * K + c);
+    return (sl >= 0 && (int64_t)sl < p.n_slots) ? sl : -1;
+  };
+
+  pdl_wait();
+  uint4 wv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = tid + k * nt;
+    if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+  }
+
+  int64_t irow = blockIdx.x;
+  int ic = 0;
+  auto issue_next = [&](int s) {
+    if (irow < p.T) {
+      if (ic < K) {
+        const int32_t sl = slot_of(irow, ic);
+        if (sl >= 0) {
+          const uint4* src = ex4 + (int64_t)sl * hv;
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            const int j = tid + k * nt;
+            if (j < hv) cp_async16(slot_addr(s, k), src + j);
+          }
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(p.residual) + irow * hv;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int j = tid + k * nt;
+          if (j < hv) cp_async16(slot_addr(s, k), src + j);
+        }
+      }
+      if (++ic > K) { ic = 0; irow += gridDim.x; }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int s = 0; s < R; ++s) issue_next(s);
+
+  int q = 0, it = 0, res_slot = 0;
+  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+    const int64_t base = row * hv;
+    // The issue cursor is about a row ahead: fetch the index and gate rows
+    // of the next two rows into L1 now, so issuing their chunks does not
+    // wait on an L2 miss.
+    if (tid < 2) {
+      const int64_t nr = row + (int64_t)(tid + 1) * gridDim.x;
+      if (nr < p.T) {
+        asm volatile("prefetch.global.L1 [%0];" :: "l"(p.index + nr * K));
+        asm volatile("prefetch.global.L1 [%0];" :: "l"(p.gates + nr * K));
+      }
+    }
+    float acc[VPT][8];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
+    uint4 rv[VPT];
+    for (int c = 0; c <= K; ++c, ++q) {
+      const int s = q % R;
+      cp_async_wait<R - 1>();
+      if (c < K) {
+        const int32_t sl = slot_of(row, c);
+        if (sl >= 0) {
+          const float gt = __ldg(p.gates + row * K + c);
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            const int j = tid + k * nt;
+            if (j < hv) {
+              const uint4 v = ld_shared_v4(slot_addr(s, k));
+              const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc[k][2 * e] = __fadd_rn(acc[k][2 * e], __fmul_rn(gt, bf_lo(xw[e])));
+                acc[k][2 * e + 1] = __fadd_rn(acc[k][2 * e + 1], __fmul_rn(gt, bf_hi(xw[e])));
+              }
+            }
+          }
+        }
+        issue_next(s);     // the adds above consumed the slot
+      } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          const int j = tid + k * nt;
+          rv[k] = make_uint4(0u, 0u, 0u, 0u);
+          if (j < hv) rv[k] = ld_shared_v4(slot_addr(s, k));
+        }
+        res_slot = s;
+      }
+    }
+    if (row + gridDim.x >= p.T) pdl_trigger();
+
+    uint4 ro[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) {
+        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        uint32_t red[4], out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
+          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+          out[e] = pack_bf16x2(s0, s1);
+          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+          ss = fmaf(q0, q0, ss);
+          ss = fmaf(q1, q1, ss);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                  make_uint4(red[0], red[1], red[2], red[3]));
+        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+      }
+    }
+    issue_next(res_slot);  // the residual's values were used above
+    ss = warp_sum(ss);
+    float* ws = warp_ss[it & 1];
+    if (lane == 0) ws[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < nwarps; ++w) tot += ws[w];
+    const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) {
+        const uint32_t qv[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
+        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint32_t n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n0 = (bf_lo(qv[e]) * rstd) * bf_lo(w[e]);
+          const float n1 = (bf_hi(qv[e]) * rstd) * bf_hi(w[e]);
+          n[e] = pack_bf16x2(n0, n1);
+        }
+        st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
+                  make_uint4(n[0], n[1], n[2], n[3]));
+      }
+    }
+  }
+  cp_async_wait<0>();
 }
 
 }  // namespace farn

@@ -73,6 +73,7 @@ class Problem:
     partial_dtype: str = "bf16"      # or "f32"
     fp8_out: bool = False            # also write norm_out as E4M3 + row scales
     norm_out: bool = True            # write the bf16 norm_out
+    kind: str = "rank_sum"           # or "moe_combine" (W = experts per token)
 
     @property
     def partial_bytes(self) -> int:
@@ -80,7 +81,11 @@ class Problem:
 
     def read_bytes(self) -> int:
         """W*T*H*pb partials + T*H*2 residual + H*2 weight (pb = 2 for bf16
-        partials, 4 for fp32)."""
+        partials, 4 for fp32); for the MoE combine the W gathered expert
+        rows of each token (bf16) plus its W int32 indices and fp32 gates."""
+        if self.kind == "moe_combine":
+            return (self.W * self.T * self.H * 2 + self.T * self.W * 8
+                    + self.T * self.H * 2 + self.H * 2)
         return self.W * self.T * self.H * self.partial_bytes + self.T * self.H * 2 + self.H * 2
 
     def write_bytes(self) -> int:
@@ -123,6 +128,8 @@ WORKLOADS = {
     "wide": [Problem("wide", 16, 4096, 7168, 1e-6, 0, Dist(NORMAL, 0.0, 1.0 / 16))],
     # residual add + RMSNorm alone (one partial: no rank sum), prefill-sized
     "rmsnorm": [Problem("rmsnorm", 1, 8192, 8192, 1e-6, 0, N01)],
+    # MoE combine of 8 experts per token at a 7168 hidden size, 4096 tokens
+    "moe_combine": [Problem("moe_combine", 8, 4096, 7168, 1e-6, 0, N01, kind="moe_combine")],
     # the prefill shape writing norm_out as E4M3 + row scales instead of bf16
     "prefill_fp8": [Problem("prefill_fp8", 8, 8192, 8192, 1e-6, 0,
                             Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
@@ -197,10 +204,29 @@ def host_f32(n: int, seed: int, stream_id: int, dist: Dist) -> np.ndarray:
     return v.astype(np.float32)
 
 
+def moe_routing(p: Problem):
+    """index int32 [T,K]: a seeded permutation of the T*K expert-output
+    rows (each used once); gates float32 [T,K]: a softmax of N(0,1) logits
+    per token."""
+    rng = np.random.default_rng(p.seed + 12345)
+    index = rng.permutation(p.T * p.W).astype(np.int32).reshape(p.T, p.W)
+    logits = rng.normal(size=(p.T, p.W))
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    gates = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+    return index, gates
+
+
 def host_inputs(p: Problem):
     """(partials list of [T,H], residual [T,H], weight [H]); partials are
-    uint16 bf16 patterns or float32, residual and weight uint16."""
+    uint16 bf16 patterns or float32, residual and weight uint16.  For the
+    MoE combine the first item is (expert_out [T*K,H], index, gates)."""
     n = p.T * p.H
+    if p.kind == "moe_combine":
+        ex = host_bf16(n * p.W, p.seed, 0, p.x).reshape(p.T * p.W, p.H)
+        index, gates = moe_routing(p)
+        res = host_bf16(n, p.seed, STREAM_RESIDUAL, p.residual).reshape(p.T, p.H)
+        w = host_bf16(p.H, p.seed, STREAM_WEIGHT, p.weight)
+        return (ex, index, gates), res, w
     if p.partial_dtype == "f32":
         xs = [host_f32(n, p.seed, r, p.x).reshape(p.T, p.H) for r in range(p.W)]
     else:
@@ -261,6 +287,16 @@ def device_inputs(p: Problem, device="cuda", seed: int | None = None):
     """Allocate and fill (partials, residual, weight) on the device."""
     import torch
     sd = p.seed if seed is None else seed
+    if p.kind == "moe_combine":
+        ex = torch.empty((p.T * p.W, p.H), dtype=torch.bfloat16, device=device)
+        fill_device(ex, sd, 0, p.x)
+        index, gates = moe_routing(p.with_seed(sd))
+        res = torch.empty((p.T, p.H), dtype=torch.bfloat16, device=device)
+        fill_device(res, sd, STREAM_RESIDUAL, p.residual)
+        w = torch.empty((p.H,), dtype=torch.bfloat16, device=device)
+        fill_device(w, sd, STREAM_WEIGHT, p.weight)
+        return ((ex, torch.from_numpy(index).to(device), torch.from_numpy(gates).to(device)),
+                res, w)
     xs = []
     xdt = torch.float32 if p.partial_dtype == "f32" else torch.bfloat16
     for r in range(p.W):

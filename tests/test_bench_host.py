@@ -79,6 +79,8 @@ def test_reference_arm_json_line(monkeypatch):
 def test_algorithmic_bytes_formula(name):
     for p in synth.workload(name):
         read = p.W * p.T * p.H * p.partial_bytes + p.T * p.H * 2 + p.H * 2
+        if p.kind == "moe_combine":           # + int32 index and fp32 gate per slot
+            read += p.T * p.W * 8
         write = (2 + p.norm_out) * p.T * p.H * 2 + (p.T * p.H + 4 * p.T) * p.fp8_out
         assert p.algorithmic_bytes() == read + write
         assert bench.call_bytes(p, p.T) == read + write

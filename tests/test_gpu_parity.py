@@ -788,3 +788,110 @@ def test_fp8_output_aliasing(dev):
                                  res.data_ptr(), w.data_ptr(), p.eps, 4, 2048, red.data_ptr(),
                                  ro.data_ptr(), nrm.data_ptr(), q.data_ptr(), 0)
     assert st == farn.FARN_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------- MoE combine
+def _moe(T, K, H, seed=3):
+    return synth.Problem("moe", K, T, H, 1e-6, seed, synth.N01, kind="moe_combine")
+
+
+def _run_moe(O, dev, p, ins=None, rows=None, ctx=None, what=""):
+    (ex, index, gates), res, w = ins if ins is not None else synth.device_inputs(p, dev)
+    out = farn.moe_combine(ex, index, gates, res, w, p.eps, ctx=ctx)
+    torch.cuda.synchronize()
+    if rows is None:
+        want = O.moe_combine(u16(ex), index.cpu().numpy(), gates.cpu().numpy(), u16(res),
+                             u16(w), p.eps)
+        got = [u16(t) for t in out]
+    else:
+        idx = torch.as_tensor(rows, device=dev)
+        want = O.moe_combine(u16(ex), index.index_select(0, idx).cpu().numpy(),
+                             gates.index_select(0, idx).cpu().numpy(),
+                             u16(res.index_select(0, idx)), u16(w), p.eps)
+        got = [u16(t.index_select(0, idx)) for t in out]
+    return assert_parity(got, want, what or f"moe T={p.T} K={p.W} H={p.H}")
+
+
+@pytest.mark.parametrize("T,K,H", [(1, 8, 7168), (5, 8, 4096), (64, 8, 7168), (300, 8, 7168),
+                                   (200, 1, 2048), (40, 32, 1024), (9, 3, 1000), (3, 6, 13)])
+def test_moe_combine(O, dev, T, K, H):
+    _run_moe(O, dev, _moe(T, K, H))
+
+
+def test_moe_combine_full_size_sampled(O, dev):
+    p = synth.workload("moe_combine")[0]
+    _run_moe(O, dev, p, rows=sample_rows(p.T, 96, seed=8))
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("env", [dict(FARN_VARIANT="generic"), dict(FARN_VPT=1),
+                                 dict(FARN_VPT=2), dict(FARN_VPT=4), dict(FARN_VARIANT="stage"),
+                                 dict(FARN_VARIANT="stage", FARN_VPT=2),
+                                 dict(FARN_VARIANT="stage", FARN_STAGE_CTAS=1)],
+                         ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
+def test_moe_combine_variants(O, dev, env):
+    ctx = make_ctx(**env)
+    try:
+        _run_moe(O, dev, _moe(33, 8, 4096, seed=9), ctx=ctx, what=f"moe {env}")
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("variant", ["row", "stage"])
+def test_moe_combine_skipped_and_bad_slots(O, dev, variant):
+    """-1 and out-of-range slots are skipped (never read); a token with no
+    valid slot gets reduced = -0."""
+    p = _moe(12, 6, 2048, seed=4)
+    (ex, index, gates), res, w = synth.device_inputs(p, dev)
+    index[0, 1] = -1
+    index[1, :] = -1
+    index[2, 3] = ex.shape[0]            # one past the end
+    index[3, 0] = 2 ** 31 - 1
+    index[4, 5] = -7
+    ctx = make_ctx(FARN_VARIANT=variant)
+    try:
+        _run_moe(O, dev, p, ins=((ex, index, gates), res, w), ctx=ctx,
+                 what=f"moe bad slots {variant}")
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("variant", ["auto", "stage"])
+def test_moe_combine_mid_size(O, dev, variant):
+    """Many rows per persistent CTA for the staged gather kernel."""
+    ctx = make_ctx(FARN_VARIANT=variant)
+    try:
+        _run_moe(O, dev, _moe(2100, 8, 7168, seed=14), ctx=ctx, what=f"moe {variant}")
+    finally:
+        ctx.close()
+
+
+def test_moe_combine_unit_gates_match_forward(O, dev):
+    """Gates of 1 and the slot layout of stacked partials: the combine and
+    the rank-sum kernel give the same bits."""
+    T, K, H = 50, 4, 4096
+    p = synth.Problem("x", K, T, H, 1e-6, 6, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    ex = torch.cat(xs, dim=0).contiguous()
+    index = torch.tensor([[k * T + t for k in range(K)] for t in range(T)], dtype=torch.int32,
+                         device=dev)
+    gates = torch.ones((T, K), dtype=torch.float32, device=dev)
+    a = farn.moe_combine(ex, index, gates, res, w, 1e-6)
+    b = farn.forward(xs, res, w, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert compare([u16(t) for t in a], [u16(t) for t in b])["norm_out"]["max_ulp"] <= 1
+
+
+def test_moe_combine_in_place_and_aliasing(O, dev):
+    p = _moe(20, 4, 2048, seed=12)
+    (ex, index, gates), res, w = synth.device_inputs(p, dev)
+    want = O.moe_combine(u16(ex), index.cpu().numpy(), gates.cpu().numpy(), u16(res), u16(w),
+                         p.eps)
+    red, nrm = torch.empty_like(res), torch.empty_like(res)
+    farn.moe_combine(ex, index, gates, res, w, p.eps, out=(red, res, nrm))
+    torch.cuda.synchronize()
+    assert_parity([u16(red), u16(res), u16(nrm)], want, "moe in place")
+    with pytest.raises(farn.FarnError) as e:       # output over an expert row
+        farn.moe_combine(ex, index, gates, res, w, p.eps, out=(ex[:20], red, nrm))
+    assert e.value.status == farn.FARN_ERR_ALIAS
