@@ -82,6 +82,12 @@ def _declare(lib):
     lib.oracle_f32_to_e4m3_sat.restype = ctypes.c_uint8
     lib.oracle_quant_e4m3_row.argtypes = [u16p, ctypes.c_int64, u8p]
     lib.oracle_quant_e4m3_row.restype = ctypes.c_float
+    lib.oracle_e2m1_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_e2m1_to_f32.restype = ctypes.c_float
+    lib.oracle_f32_to_e2m1_sat.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_e2m1_sat.restype = ctypes.c_uint8
+    lib.oracle_quant_nvfp4_row.argtypes = [u16p, ctypes.c_int64, ctypes.c_float, u8p, u8p]
+    lib.oracle_quant_nvfp4_row.restype = None
     lib.oracle_moe_combine.argtypes = [u16p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_float), ctypes.c_int, u16p,
                                        u16p, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
@@ -220,6 +226,34 @@ def _Oracle_e4m3_to_f32(self, b: int) -> float:
     return float(self.lib.oracle_e4m3_to_f32(int(b)))
 
 
+def _Oracle_quant_nvfp4(self, norm, g: float):
+    """NVFP4 quantisation of bf16 norm_out rows [T,H] (H % 16 == 0) under
+    the tensor scale g: (q uint8 [T,H/2], two E2M1 codes per byte, even
+    element in the low nibble; s uint8 [T,H/16], E4M3 block scales)."""
+    norm = _u16(norm)
+    if norm.ndim == 1:
+        norm = norm[None, :]
+    T, H = norm.shape
+    if H % 16:
+        raise ValueError("NVFP4 needs H % 16 == 0")
+    q = np.empty((T, H // 2), np.uint8)
+    s = np.empty((T, H // 16), np.uint8)
+    u8 = ctypes.POINTER(ctypes.c_uint8)
+    for t in range(T):
+        row = np.ascontiguousarray(norm[t])
+        self.lib.oracle_quant_nvfp4_row(_p(row), H, float(np.float32(g)),
+                                        q[t].ctypes.data_as(u8), s[t].ctypes.data_as(u8))
+    return q, s
+
+
+def _Oracle_e2m1(self, f: float) -> int:
+    return int(self.lib.oracle_f32_to_e2m1_sat(float(np.float32(f))))
+
+
+def _Oracle_e2m1_to_f32(self, c: int) -> float:
+    return float(self.lib.oracle_e2m1_to_f32(int(c)))
+
+
 def _Oracle_moe_combine(self, expert_out, index, gates, residual, weight, eps: float):
     """MoE combine + residual + RMSNorm: expert_out uint16 [S,H], index
     int32 [T,K], gates float32 [T,K], residual uint16 [T,H], weight [H]."""
@@ -255,6 +289,9 @@ Oracle.moe_combine_acc = _Oracle_moe_combine_acc
 Oracle.quant_e4m3 = _Oracle_quant
 Oracle.f32_to_e4m3 = _Oracle_e4m3
 Oracle.e4m3_to_f32 = _Oracle_e4m3_to_f32
+Oracle.quant_nvfp4 = _Oracle_quant_nvfp4
+Oracle.f32_to_e2m1 = _Oracle_e2m1
+Oracle.e2m1_to_f32 = _Oracle_e2m1_to_f32
 
 
 def forward(xs, residual, weight, eps: float):

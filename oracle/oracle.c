@@ -279,6 +279,94 @@ float oracle_quant_e4m3_row(const uint16_t *norm, int64_t H, uint8_t *q)
 }
 
 /* ---------------------------------------------------------------------
+ * Fused NVFP4 quantisation of norm_out (also not described by the page:
+ * the 4-bit input of a block-scaled GEMM).
+ *
+ * E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; magnitudes
+ * 0, 0.5 (the one subnormal), 1, 1.5, 2, 3, 4, 6; no infinities, no NaN.
+ * NVFP4 groups 16 consecutive elements of a row into a block that shares
+ * one positive E4M3 scale, under one fp32 scale for the whole tensor.
+ *
+ * Reading: the tensor scale g (fp32, finite, > 0) is an input of the call
+ * (a calibrated constant: a fused kernel cannot see the whole tensor's
+ * amax before it writes the first block).  For block b of row t
+ * (elements 16b .. 16b+15):
+ *     amax   = the largest |norm_out| of the block (NaN ignored)
+ *     s[t,b] = E4M3((amax / 6) * g)            saturating, as above
+ *     inv    = g / e4m3_value(s[t,b])           one fp32 division
+ *     q[t,h] = E2M1(norm_out[t,h] * inv)        round to nearest even,
+ *              magnitudes above 6 (infinity included) saturated to 6
+ * and q = 0 for the whole block when e4m3_value(s) is 0 (an all-zero block
+ * or one whose scale underflows).  A NaN element, which E2M1 cannot hold,
+ * is written as +6 (code 0x7).  The value represented is
+ * e2m1_value(q) * e4m3_value(s) / g.
+ * Layout: q packs two codes per byte, element 2i in the low nibble and
+ * element 2i+1 in the high nibble ([T, H/2] bytes); s is [T, H/16] bytes.
+ * ------------------------------------------------------------------- */
+float oracle_e2m1_to_f32(uint8_t c)
+{
+    float sign = (c & 0x8u) ? -1.0f : 1.0f;
+    int e = (c >> 1) & 0x3, m = c & 0x1;
+    if (e == 0)
+        return sign * 0.5f * (float)m;
+    return sign * ldexpf(1.0f + 0.5f * (float)m, e - 1);
+}
+
+uint8_t oracle_f32_to_e2m1_sat(float f)
+{
+    if (isnan(f))
+        return 0x7u;
+    uint8_t sign = signbit(f) ? 0x8u : 0x0u;
+    float a = fabsf(f);
+    if (a > 6.0f)
+        return (uint8_t)(sign | 0x7u);           /* saturate to 6 */
+    if (a == 0.0f)
+        return sign;
+    int e2;
+    frexpf(a, &e2);                 /* a = m * 2^e2, m in [0.5, 1) */
+    int E = e2 - 1;                 /* 2^E <= a < 2^(E+1) */
+    if (E < 0)
+        E = 0;                      /* below 1: the subnormal step 0.5 */
+    float step = ldexpf(1.0f, E - 1);
+    float v = rintf(a / step) * step;   /* exact division; nearest even */
+    if (v > 6.0f)
+        v = 6.0f;
+    if (v == 0.0f)
+        return sign;
+    if (v < 1.0f)
+        return (uint8_t)(sign | 0x1u);           /* 0.5 */
+    frexpf(v, &e2);
+    E = e2 - 1;
+    int mant = (int)((v / ldexpf(1.0f, E) - 1.0f) * 2.0f);
+    return (uint8_t)(sign | (uint8_t)((E + 1) << 1) | (uint8_t)mant);
+}
+
+/* One row (H a multiple of 16): writes q[0..H/2) and s[0..H/16). */
+void oracle_quant_nvfp4_row(const uint16_t *norm, int64_t H, float g, uint8_t *q, uint8_t *s)
+{
+    for (int64_t b = 0; b < H / 16; ++b) {
+        const uint16_t *blk = norm + 16 * b;
+        float amax = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            float v = fabsf(oracle_bf16_to_f32(blk[i]));
+            if (v > amax)           /* NaN never compares greater */
+                amax = v;
+        }
+        s[b] = oracle_f32_to_e4m3_sat((amax / 6.0f) * g);
+        float sv = oracle_e4m3_to_f32(s[b]);
+        float inv = sv > 0.0f ? g / sv : 0.0f;
+        for (int i = 0; i < 16; i += 2) {
+            uint8_t lo = 0, hi = 0;
+            if (sv > 0.0f) {
+                lo = oracle_f32_to_e2m1_sat(oracle_bf16_to_f32(blk[i]) * inv);
+                hi = oracle_f32_to_e2m1_sat(oracle_bf16_to_f32(blk[i + 1]) * inv);
+            }
+            q[8 * b + i / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------
  * MoE combine ("local y reduce": the per-token weighted sum of its top-k
  * expert outputs) fused with the same residual add + RMSNorm.  The page
  * names the step but defines neither its weights nor its layout; reading:

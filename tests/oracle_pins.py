@@ -504,6 +504,156 @@ def pin_quant_row_vs_exact_rounding(O):
             assert int(q[t][h]) == e4m3_exact(Fraction(float(d)) if d != 0 else float(d))
 
 
+# ------------------------------------------------------ NVFP4 quantisation
+# E2M1 magnitudes by code (bits: exponent 2, fraction 1, bias 1), written
+# out from the format definition: 0, the subnormal 0.5, then 2^(e-1)(1+m/2).
+E2M1_GRID = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2),
+             Fraction(2), Fraction(3), Fraction(4), Fraction(6)]
+
+
+def e2m1_exact(q) -> int:
+    """Exact rational (or float special) -> E2M1 code by exhaustive search
+    of the eight magnitudes: the nearest, a tie going to the code with an
+    even fraction bit; magnitudes above 6 and infinities give 6; NaN gives
+    +6 (the reading: E2M1 has no NaN)."""
+    if isinstance(q, float):
+        if np.isnan(q):
+            return 0x7
+        if np.isinf(q):
+            return 0xF if q < 0 else 0x7
+        if q == 0.0:
+            return 0x8 if np.signbit(q) else 0x0
+        q = Fraction(q)
+    sign = 0x8 if q < 0 else 0
+    a = abs(q)
+    best = None
+    for code, g in enumerate(E2M1_GRID):
+        d = abs(a - g)
+        if best is None or d < best[0] or (d == best[0] and code % 2 == 0):
+            best = (d, code)
+    return sign | best[1]
+
+
+def pin_e2m1_decode_all_patterns(O):
+    for c in range(16):
+        want = E2M1_GRID[c & 7]
+        want = -want if c & 8 else want
+        got = O.e2m1_to_f32(c)
+        assert Fraction(got) == want and (np.signbit(got) == bool(c & 8)), hex(c)
+
+
+def pin_e2m1_rounding_vs_exact(O):
+    rng = np.random.default_rng(61)
+    vals = list((rng.normal(size=2000) * np.exp2(rng.integers(-4, 4, 2000))).astype(np.float32))
+    # every midpoint between neighbours and its two fp32 neighbours, saturation edges
+    for lo, hi in zip(E2M1_GRID[:-1], E2M1_GRID[1:]):
+        mid = np.float32(float((lo + hi) / 2))
+        for sgn in (1, -1):
+            vals += [np.float32(sgn * mid), np.float32(sgn * np.nextafter(mid, np.float32(0))),
+                     np.float32(sgn * np.nextafter(mid, np.float32(10)))]
+    vals += [np.float32(v) for v in (6, 6.5, 7, 8, 1e30, -1e30, 2.0 ** -126, 0.0, -0.0,
+                                      float("inf"), float("-inf"), 0.2499999, 5.0000005)]
+    for v in vals:
+        got = O.f32_to_e2m1(float(v))
+        want = e2m1_exact(float(v) if (v == 0 or not np.isfinite(v)) else Fraction(float(v)))
+        assert got == want, (float(v), hex(got), hex(want))
+    assert O.f32_to_e2m1(float("nan")) == 0x7
+
+
+def _nvfp4_decode(O, q, s, g, H):
+    """Dequantised values e2m1(q) * e4m3(s) / g in exact rationals."""
+    out = []
+    for h in range(H):
+        byte = int(q[h // 2])
+        code = (byte >> 4) if h % 2 else (byte & 0xF)
+        out.append(Fraction(O.e2m1_to_f32(code)) * Fraction(O.e4m3_to_f32(int(s[h // 16])))
+                   / Fraction(float(np.float32(g))))
+    return out
+
+
+def pin_nvfp4_block_closed_forms(O):
+    B = bx.bits
+    # g = 1, amax 6: the block scale is E4M3(1) and the values are their own codes
+    row = np.array([B(6), B(-3), B(1.5), B(0.5), B(1), B(-0.5), B(4), B(2)] + [0] * 8, np.uint16)
+    q, s = O.quant_nvfp4(row, 1.0)
+    assert s[0][0] == 0x38                              # 1.0 = 2^0: exponent field 7
+    assert list(q[0][:4]) == [0x7 | (0xD << 4), 0x3 | (0x1 << 4),
+                              0x2 | (0x9 << 4), 0x6 | (0x4 << 4)]
+    assert not q[0][4:].any()
+    # amax 12 with g = 1: scale 2, every value halved before rounding
+    row = np.array([B(12), B(-5), B(3), B(1)] + [0] * 12, np.uint16)
+    q, s = O.quant_nvfp4(row, 1.0)
+    assert O.e4m3_to_f32(int(s[0][0])) == 2.0
+    assert [Fraction(v) for v in _nvfp4_decode(O, q[0], s[0], 1.0, 4)] == [12, -4, 3, 1]
+    # the tensor scale g multiplies the block scale and cancels on decode
+    q2, s2 = O.quant_nvfp4(row, 64.0)
+    assert O.e4m3_to_f32(int(s2[0][0])) == 128.0 and np.array_equal(q, q2)
+    # an all-zero block: scale 0, codes 0; a block whose scale underflows: codes 0
+    tiny = np.array([B(2.0 ** -20)] * 16, np.uint16)
+    q, s = O.quant_nvfp4(np.concatenate([np.zeros(16, np.uint16), tiny]), 1.0)
+    assert not s.any() and not q.any()
+    # NaN: ignored by the block amax, written as +6; infinity saturates
+    row = np.array([bx.QNAN, B(3), B(-6), 0xFF80] + [0] * 12, np.uint16)   # 0xFF80 = -inf
+    q, s = O.quant_nvfp4(row, 1.0)
+    assert O.e4m3_to_f32(int(s[0][0])) == 448.0          # (inf / 6) * 1 saturates
+    assert (q[0][0] & 0xF) == 0x7 and (q[0][1] >> 4) == 0xF
+    # blocks are independent: a large block leaves its neighbour alone
+    a = np.array([B(1)] * 16, np.uint16)
+    b = np.array([B(1000)] * 16, np.uint16)
+    qa, sa = O.quant_nvfp4(a, 1.0)
+    qab, sab = O.quant_nvfp4(np.concatenate([a, b]), 1.0)
+    assert np.array_equal(qab[0][:8], qa[0]) and sab[0][0] == sa[0][0]
+
+
+def pin_nvfp4_vs_exact_rounding(O):
+    """s = E4M3(fp32(fp32(amax / 6) * g)), inv = fp32(g / e4m3(s)),
+    q = E2M1(fp32(v * inv)), each conversion taken exactly from rationals."""
+    rng = np.random.default_rng(67)
+    for trial in range(6):
+        H = 16 * int(rng.integers(1, 6))
+        mag = np.exp2(rng.integers(-6, 6, size=(3, H // 16))).repeat(16, axis=1)
+        x = (rng.normal(size=(3, H)) * mag).astype(np.float32)
+        rows = (x.view(np.uint32) >> 16).astype(np.uint16)
+        g = np.float32(np.exp2(rng.uniform(-4, 8)))
+        q, s = O.quant_nvfp4(rows, float(g))
+        for t in range(3):
+            vals = bx.to_f64(rows[t])
+            for b in range(H // 16):
+                blk = vals[16 * b:16 * b + 16]
+                amax = np.float32(np.abs(blk).max())
+                sc = e4m3_exact(Fraction(float(np.float32(np.float32(amax / np.float32(6)) * g))))
+                assert int(s[t][b]) == sc, (trial, t, b)
+                sv = Fraction(O.e4m3_to_f32(sc))
+                for i in range(16):
+                    h = 16 * b + i
+                    code = (int(q[t][h // 2]) >> 4) if h % 2 else (int(q[t][h // 2]) & 0xF)
+                    if sv == 0:
+                        assert code == 0
+                        continue
+                    inv = np.float32(g / np.float32(float(sv)))
+                    d = np.float32(np.float32(blk[i]) * inv)
+                    want = e2m1_exact(Fraction(float(d)) if d != 0 else float(d))
+                    assert code == want, (trial, t, h, hex(code), hex(want))
+
+
+def pin_nvfp4_power_of_two_invariance(O):
+    """Scaling a row (or g) by 2^k scales every decoded block scale by 2^k
+    and leaves the codes unchanged, while the scales stay normal E4M3."""
+    rng = np.random.default_rng(71)
+    x = rng.normal(size=(4, 64)).astype(np.float32)
+    base = (x.view(np.uint32) >> 16).astype(np.uint16)
+    q0, s0 = O.quant_nvfp4(base, 16.0)
+    d0 = np.array([[O.e4m3_to_f32(int(v)) for v in r] for r in s0])
+    for k in (-2, 3):
+        xs = ((x * np.float32(2.0 ** k)).view(np.uint32) >> 16).astype(np.uint16)
+        q1, s1 = O.quant_nvfp4(xs, 16.0)
+        d1 = np.array([[O.e4m3_to_f32(int(v)) for v in r] for r in s1])
+        assert np.array_equal(q0, q1) and np.array_equal(d1, d0 * 2.0 ** k)
+        q2, s2 = O.quant_nvfp4(base, 16.0 * 2.0 ** k)
+        d2 = np.array([[O.e4m3_to_f32(int(v)) for v in r] for r in s2])
+        assert np.array_equal(q0, q2) and np.array_equal(d2, d0 * 2.0 ** k)
+
+
 # ---------------------------------------------------------------- MoE combine
 def _f32(q: Fraction) -> Fraction:
     """Exact rational rounded to the nearest fp32 (ties to even)."""

@@ -75,6 +75,14 @@ MUTANTS = {
     "combine_gate_index_wrong": ("gates_row[k] * oracle", "gates_row[0] * oracle"),
     "combine_no_range_check": ("if (s < 0 || (int64_t)s >= n_slots)", "if (s < 0)"),
     "combine_slot_row_wrong": ("expert_out[(int64_t)s * H + h]", "expert_out[(int64_t)s + h]"),
+    "e2m1_ties_away": ("float v = rintf(a / step) * step;", "float v = roundf(a / step) * step;"),
+    "e2m1_wrong_bias": ("(uint8_t)((E + 1) << 1)", "(uint8_t)((E + 2) << 1)"),
+    "nvfp4_nibbles_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "nvfp4_half_block_amax": ("for (int i = 0; i < 16; ++i) {", "for (int i = 0; i < 8; ++i) {"),
+    "nvfp4_tensor_scale_inverted": ("float inv = sv > 0.0f ? g / sv : 0.0f;",
+                                    "float inv = sv > 0.0f ? 1.0f / (sv * g) : 0.0f;"),
+    "nvfp4_scale_without_tensor_scale": ("oracle_f32_to_e4m3_sat((amax / 6.0f) * g)",
+                                         "oracle_f32_to_e4m3_sat(amax / 6.0f)"),
     "widen_drops_low_bit": (
         "uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)(b & 0xFFFEu)) << 16;"),
 }
