@@ -58,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["decode", "c1", "prefill", "nonpow2", "wide", "rmsnorm",
-                             "prefill_f32", "prefill_fp8", "moe_combine"])
+                             "prefill_f32", "prefill_fp8", "prefill_nvfp4", "moe_combine"])
     ap.add_argument("--in-place", action="store_true",
                     help="write residual_out over the residual (in-place residual update)")
     ap.add_argument("--impl", default="farn", choices=["farn", "reference"])
@@ -231,6 +231,8 @@ def time_oracle_rows(sample, rows_total_target=None, seconds=10.0):
                 outs = O.forward(xs, res, w, p.eps)
             if p.fp8_out:
                 O.quant_e4m3(outs[2])
+            if p.nvfp4_out:
+                O.quant_nvfp4(outs[2], p.tensor_scale)
             r = res.shape[0]
             nbytes += call_bytes(p, r)
             nrows += r
@@ -281,6 +283,8 @@ def run_reference(args):
                 outs = O.forward([x[t:t + 1] for x in xs], res[t:t + 1], w, p.eps)
             if p.fp8_out:
                 O.quant_e4m3(outs[2])
+            if p.nvfp4_out:
+                O.quant_nvfp4(outs[2], p.tensor_scale)
             b += call_bytes(p, 1)
             n += 1
         return b, n
@@ -320,8 +324,18 @@ def workload_desc(name, problems):
     if name == "decode":
         return (f"decode sweep: W={p.W}, H={p.H}, T in "
                 f"{{{','.join(str(q.T) for q in problems)}}} (one call per T), eps={p.eps:g}")
+    out = ""
+    if p.fp8_out:
+        out = ", norm_out written as E4M3 + fp32 row scales (no bf16 norm_out)"
+    elif p.nvfp4_out:
+        out = (", norm_out written as NVFP4: E2M1 codes + E4M3 scales per 16 elements, "
+               f"tensor scale {p.tensor_scale:g} (no bf16 norm_out)")
+    if p.kind == "moe_combine":
+        out = (f", MoE combine of K={p.W} gathered expert rows per token "
+               "(seeded permutation, softmax gates)")
     return (f"{name}: W={p.W}, T={p.T}, H={p.H}, x ~ {p.x.describe()}, "
-            f"residual ~ {p.residual.describe()}, weight ~ {p.weight.describe()}, eps={p.eps:g}")
+            f"residual ~ {p.residual.describe()}, weight ~ {p.weight.describe()}, eps={p.eps:g}"
+            + out)
 
 
 # ------------------------------------------------------------------ GPU
@@ -483,7 +497,12 @@ def run_gpu(args):
         c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
         c["frac"] = c["gbs"] / peak
         if problems[j].kind == "moe_combine":
-            c["variant"] = "combine (one CTA per row, gathered rows)"
+            _, (ex, _, _), res_j, w_j, outs_j = sets[0][j]
+            v, thr = farn.farn_plan_moe_combine(
+                ctx.handle, problems[j].W, problems[j].T, problems[j].H, ex.data_ptr(),
+                res_j.data_ptr(), w_j.data_ptr(), outs_j[0].data_ptr(), outs_j[1].data_ptr(),
+                outs_j[2].data_ptr())
+            c["variant"] = ("combine-stage" if v == "stage" else v) + f" threads={thr}"
             continue
         v, cs, thr = farn.farn_plan_typed(ctx.handle, *plan_args(sets[0][j]))
         c["variant"] = f"{v} cluster={cs} threads={thr}"
@@ -545,7 +564,8 @@ def run_gpu(args):
 
 KERNELS = {"row": "farn_vec_kernel", "cluster": "farn_vec_kernel",
            "generic": "farn_generic_kernel", "bulk": "farn_bulk_kernel",
-           "stage": "farn_stage_kernel", "combine": "farn_combine_kernel"}
+           "stage": "farn_stage_kernel", "combine": "farn_combine_kernel",
+           "combine-stage": "farn_combine_stage_kernel"}
 KERNEL_SOURCES = ("rank_sum_residual_gb300/csrc/farn_kernels.cuh",)
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
 
@@ -592,11 +612,13 @@ def plan_args(call):
             [x.data_ptr() for x in xs], res.data_ptr(), w.data_ptr(),
             outs[0].data_ptr(), outs[1].data_ptr(),
             outs[2].data_ptr() if outs[2] is not None else 0,
-            farn.FARN_PLAN_FP8_OUT if p.fp8_out else 0)
+            farn.FARN_PLAN_FP8_OUT if p.fp8_out else
+            (farn.FARN_PLAN_NVFP4_OUT if p.nvfp4_out else 0))
 
 
 def make_outputs(p, dev):
-    """(reduced, residual_out, norm_out or None[, E4M3 bytes, row scales])."""
+    """(reduced, residual_out, norm_out or None[, E4M3 bytes, row scales |
+    E2M1 code bytes, E4M3 block scales])."""
     import torch
     outs = [torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     outs.append(torch.empty((p.T, p.H), dtype=torch.bfloat16, device=dev)
@@ -604,6 +626,9 @@ def make_outputs(p, dev):
     if p.fp8_out:
         outs.append(torch.empty((p.T, p.H), dtype=torch.uint8, device=dev))
         outs.append(torch.empty((p.T,), dtype=torch.float32, device=dev))
+    if p.nvfp4_out:
+        outs.append(torch.empty((p.T, p.H // 2), dtype=torch.uint8, device=dev))
+        outs.append(torch.empty((p.T, p.H // 16), dtype=torch.uint8, device=dev))
     return tuple(outs)
 
 
@@ -614,10 +639,20 @@ def call_forward(p, xs, res, w, outs, ctx, stream):
         ex, index, gates = xs
         farn.moe_combine(ex, index, gates, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
         return
-    if not p.fp8_out:
+    if not p.fp8_out and not p.nvfp4_out:
         farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx, stream=stream)
         return
     s = stream if stream is not None else __import__("torch").cuda.current_stream()
+    if p.nvfp4_out:
+        st = farn.farn_forward_nvfp4(
+            (ctx or farn._context_for(res.device.index)).handle, [x.data_ptr() for x in xs],
+            farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16, len(xs), res.data_ptr(),
+            w.data_ptr(), p.eps, p.T, p.H, p.tensor_scale, outs[0].data_ptr(),
+            outs[1].data_ptr(), outs[2].data_ptr() if outs[2] is not None else 0,
+            outs[3].data_ptr(), outs[4].data_ptr(), s.cuda_stream)
+        if st != farn.FARN_OK:
+            raise farn.FarnError(st, "farn_forward_nvfp4")
+        return
     st = farn.farn_forward_quant(
         (ctx or farn._context_for(res.device.index)).handle, [x.data_ptr() for x in xs],
         farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16, len(xs), res.data_ptr(),
@@ -728,6 +763,9 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
             if p.fp8_out:
                 outs.append(take(dev_out, "out", n, torch.uint8, (p.T, p.H)))
                 outs.append(take(dev_out, "out", 4 * p.T, torch.float32, (p.T,)))
+            if p.nvfp4_out:
+                outs.append(take(dev_out, "out", n // 2, torch.uint8, (p.T, p.H // 2)))
+                outs.append(take(dev_out, "out", n // 16, torch.uint8, (p.T, p.H // 16)))
             views.append((p, xs, res, w, tuple(outs)))
         slots.append((dev_in, dev_out, views))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

@@ -222,6 +222,38 @@ int farn_forward_quant(const farn_ctx *ctx,
                        void *norm_q, float *row_scale,
                        cudaStream_t stream);
 
+/* farn_forward_typed plus an NVFP4 copy of norm_out, the 4-bit input of a
+ * block-scaled GEMM.  (Not described by the page either.)  Each block of 16
+ * consecutive elements of a row, b = h / 16, shares one E4M3 scale under
+ * the fp32 tensor scale g = tensor_scale (a calibrated input: a fused
+ * kernel cannot see the whole tensor before it writes its first block):
+ *     amax            = max of |norm_out| over the block (NaN ignored)
+ *     block_scale[t,b] = E4M3((amax / 6) * g)            (saturating)
+ *     inv             = g / value(block_scale[t,b])      (fp32 division)
+ *     code[t,h]       = E2M1(norm_out[t,h] * inv)
+ * E2M1 has 1 sign, 2 exponent and 1 fraction bit (magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6); the conversion rounds to nearest even and saturates
+ * larger magnitudes and infinities to +-6; a NaN element is written as +6
+ * (code 7); a block whose scale is 0 gets all-zero codes.  The value a code
+ * stands for is value(code) * value(block_scale) / g.
+ *   norm_fp4     uint8 [T, H/2]: codes of elements 2i (low nibble) and
+ *                2i+1 (high nibble) in byte i; 4-byte aligned for the
+ *                fast kernels
+ *   block_scale  uint8 [T, H/16] (E4M3 patterns, row-major, no swizzle)
+ *   tensor_scale finite, > 0
+ *   norm_out     bf16 [T,H], or NULL to skip writing it
+ *   H            a multiple of 16
+ * The other arguments, checks and errors are those of farn_forward_typed
+ * (FARN_ERR_INVALID_ARG also for H % 16 != 0 or a bad tensor_scale);
+ * norm_fp4 and block_scale take part in the aliasing checks. */
+int farn_forward_nvfp4(const farn_ctx *ctx,
+                       const void *const *partials, int partial_dtype, int W,
+                       const void *residual, const void *weight, float eps,
+                       int64_t T, int64_t H, float tensor_scale,
+                       void *reduced_out, void *residual_out, void *norm_out,
+                       void *norm_fp4, void *block_scale,
+                       cudaStream_t stream);
+
 /* farn_moe_combine - the MoE "local y reduce" fused with the same
  * residual add + RMSNorm.  (The page names the per-token reduction of
  * expert outputs but defines neither its weights nor its layout; this is
@@ -245,12 +277,26 @@ int farn_moe_combine(const farn_ctx *ctx,
                      void *reduced_out, void *residual_out, void *norm_out,
                      cudaStream_t stream);
 
+/* Which kernel farn_moe_combine would launch for this shape and these
+ * pointers, without launching: 2 generic (any H or alignment), 4 stage
+ * (persistent CTAs that gather the rows into shared memory with cp.async;
+ * long inputs), 5 combine (one CTA per row).  *threads receives the threads
+ * per CTA.  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
+ * NULL pointer; aliasing is not checked). */
+int farn_plan_moe_combine(const farn_ctx *ctx, int K, int64_t T, int64_t H,
+                          const void *expert_out, const void *residual,
+                          const void *weight, const void *reduced_out,
+                          const void *residual_out, const void *norm_out,
+                          int *variant, int *threads);
+
 /* Flags of farn_plan_typed. */
 #define FARN_PLAN_FP8_OUT 1   /* the call also writes the FP8 norm output */
+#define FARN_PLAN_NVFP4_OUT 2 /* the call also writes the NVFP4 norm output */
 
 /* farn_plan for partials of type `partial_dtype` (a farn_dtype), for a
- * farn_forward_typed call (flags 0) or a farn_forward_quant call
- * (FARN_PLAN_FP8_OUT; norm_out may then be NULL).  Only shape, dtype,
+ * farn_forward_typed call (flags 0), a farn_forward_quant call
+ * (FARN_PLAN_FP8_OUT) or a farn_forward_nvfp4 call (FARN_PLAN_NVFP4_OUT);
+ * with either flag norm_out may be NULL.  Only shape, dtype,
  * flags and pointer alignment matter; aliasing is not checked.  Returns
  * FARN_ERR_INVALID_ARG for a bad shape, dtype, flag or NULL pointer. */
 int farn_plan_typed(const farn_ctx *ctx, int partial_dtype, int flags, int W,

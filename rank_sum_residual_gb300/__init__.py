@@ -37,7 +37,7 @@ FARN_ERR_UNSUPPORTED = -2
 FARN_ERR_ALIAS = -3
 FARN_ERR_CUDA = -4
 FARN_ERR_NOMEM = -5
-VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk", 4: "stage"}
+VARIANTS = {0: "row", 1: "cluster", 2: "generic", 3: "bulk", 4: "stage", 5: "combine"}
 FARN_BF16, FARN_F32 = 0, 1
 
 _lib = None
@@ -71,6 +71,9 @@ def _load():
         lib.farn_forward_quant.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64,
                                            vp, vp, vp, vp, vp, vp]
         lib.farn_forward_quant.restype = i32
+        lib.farn_forward_nvfp4.argtypes = [vp, pvp, i32, i32, cvp, cvp, f32, i64, i64, f32,
+                                           vp, vp, vp, vp, vp, vp]
+        lib.farn_forward_nvfp4.restype = i32
         lib.farn_moe_combine.argtypes = [vp, cvp, i64, cvp, cvp, i32, cvp, cvp, f32, i64, i64,
                                          vp, vp, vp, vp]
         lib.farn_moe_combine.restype = i32
@@ -85,6 +88,9 @@ def _load():
                                         cvp, cvp, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                         ctypes.POINTER(i32)]
         lib.farn_plan_typed.restype = i32
+        lib.farn_plan_moe_combine.argtypes = [vp, i32, i64, i64, cvp, cvp, cvp, cvp, cvp, cvp,
+                                              ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.farn_plan_moe_combine.restype = i32
         lib.farn_forward_noalloc.argtypes = [i32, pvp, i32, cvp, cvp, f32, i64, i64,
                                              vp, vp, vp, vp, ctypes.POINTER(i32)]
         lib.farn_forward_noalloc.restype = i32
@@ -157,6 +163,20 @@ def farn_forward_quant(ctx, partials, partial_dtype, W, residual, weight, eps, T
         ctypes.c_void_p(int(residual_out)),
         ctypes.c_void_p(int(norm_out)) if norm_out else None,
         ctypes.c_void_p(int(norm_q)), ctypes.c_void_p(int(row_scale)),
+        ctypes.c_void_p(int(stream)))
+
+
+def farn_forward_nvfp4(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                       tensor_scale, reduced_out, residual_out, norm_out, norm_fp4,
+                       block_scale, stream=0) -> int:
+    """C ``farn_forward_nvfp4``: also writes norm_out as NVFP4 (two E2M1
+    codes per byte, one E4M3 scale per 16 elements, under tensor_scale);
+    norm_out may be 0 to skip it."""
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    return _load().farn_forward_nvfp4(
+        ctypes.c_void_p(ctx) if ctx else None, _ptr_array(partials), int(partial_dtype),
+        int(W), v(residual), v(weight), float(eps), int(T), int(H), float(tensor_scale),
+        v(reduced_out), v(residual_out), v(norm_out), v(norm_fp4), v(block_scale),
         ctypes.c_void_p(int(stream)))
 
 
@@ -252,6 +272,7 @@ def farn_plan(ctx, W, T, H, partials, residual, weight, reduced_out,
 
 
 FARN_PLAN_FP8_OUT = 1
+FARN_PLAN_NVFP4_OUT = 2
 
 
 def farn_plan_typed(ctx, partial_dtype, W, T, H, partials, residual, weight, reduced_out,
@@ -267,6 +288,20 @@ def farn_plan_typed(ctx, partial_dtype, W, T, H, partials, residual, weight, red
     if st != FARN_OK:
         raise FarnError(st, "farn_plan_typed")
     return VARIANTS[variant.value], cs.value, thr.value
+
+
+def farn_plan_moe_combine(ctx, K, T, H, expert_out, residual, weight, reduced_out,
+                          residual_out, norm_out):
+    """C ``farn_plan_moe_combine``: (variant name, threads per CTA)."""
+    variant, thr = ctypes.c_int(), ctypes.c_int()
+    v = lambda a: ctypes.c_void_p(int(a)) if a else None  # noqa: E731
+    st = _load().farn_plan_moe_combine(ctypes.c_void_p(ctx), int(K), int(T), int(H),
+                                       v(expert_out), v(residual), v(weight), v(reduced_out),
+                                       v(residual_out), v(norm_out), ctypes.byref(variant),
+                                       ctypes.byref(thr))
+    if st != FARN_OK:
+        raise FarnError(st, "farn_plan_moe_combine")
+    return VARIANTS[variant.value], thr.value
 
 
 class Context:
@@ -396,3 +431,40 @@ def forward_quant(partials, residual, weight, eps: float, write_norm: bool = Tru
         raise FarnError(st, "farn_forward_quant")
     return red, ro, nrm, q, scale
 
+
+def forward_nvfp4(partials, residual, weight, eps: float, tensor_scale: float,
+                  write_norm: bool = True, ctx=None, stream=None):
+    """``forward`` plus the NVFP4 copy of norm_out.  Returns (reduced,
+    residual_out, norm_out or None, norm_fp4 uint8 [T,H/2] (two E2M1 codes
+    per byte, the even element in the low nibble), block_scale uint8
+    [T,H/16] (E4M3 patterns)).  H must be a multiple of 16."""
+    import torch
+    partials = list(partials)
+    if not partials:
+        raise ValueError("partials must hold at least one tensor")
+    T, H = residual.shape
+    if H % 16:
+        raise ValueError(f"NVFP4 output needs H % 16 == 0, got H = {H}")
+    dev = residual.device
+    pdt = partials[0].dtype
+    if pdt not in (torch.bfloat16, torch.float32):
+        raise TypeError(f"partials must be bfloat16 or float32, got {pdt}")
+    for r, x in enumerate(partials):
+        _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
+    _check_tensor(residual, "residual", (T, H), dev)
+    _check_tensor(weight, "weight", (H,), dev)
+    red = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    nrm = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None
+    q = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
+    sc = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
+    c = ctx if ctx is not None else _context_for(dev.index)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = farn_forward_nvfp4(c.handle, [x.data_ptr() for x in partials],
+                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
+                            residual.data_ptr(), weight.data_ptr(), eps, T, H, tensor_scale,
+                            red.data_ptr(), ro.data_ptr(), nrm.data_ptr() if nrm is not None else 0,
+                            q.data_ptr(), sc.data_ptr(), s.cuda_stream)
+    if st != FARN_OK:
+        raise FarnError(st, "farn_forward_nvfp4")
+    return red, ro, nrm, q, sc

@@ -27,6 +27,7 @@ enum {
   kVariantGeneric = 2,
   kVariantBulk = 3,
   kVariantStage = 4,
+  kVariantCombine = 5,   // the MoE combine's one-CTA-per-row gather kernel
   kVariantAuto = -1
 };
 
@@ -45,8 +46,8 @@ struct farn_ctx {
   int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
   int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
   int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
-  int stage_regs[3][2];  // registers per thread of the staged kernels
-                         // [plain, FP8 output, MoE combine][4 vectors]
+  int stage_regs[4][2];  // registers per thread of the staged kernels
+                         // [plain, FP8, MoE combine, NVFP4][4 vectors]
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
 };
@@ -60,25 +61,30 @@ typedef void (*VecKernel)(const farn::Params);
 // H = 8192).
 constexpr int kStageDepths[4] = {16, 12, 8, 6};
 
-template <bool Q>
+// Quantised copy of norm_out written alongside (the stage kernel's QM).
+enum { kQuantNone = 0, kQuantFp8 = 1, kQuantNvfp4 = 2 };
+
+template <int QM>
 VecKernel pick_stage_q(int vpt, int r) {
   if (vpt == 2) {
-    if (r == 8) return &farn::farn_stage_kernel<2, 8, Q>;
-    if (r == 12) return &farn::farn_stage_kernel<2, 12, Q>;
-    if (r == 16) return &farn::farn_stage_kernel<2, 16, Q>;
-    if (Q && r == 6) return &farn::farn_stage_kernel<2, 6, true>;
+    if (r == 8) return &farn::farn_stage_kernel<2, 8, QM>;
+    if (r == 12) return &farn::farn_stage_kernel<2, 12, QM>;
+    if (r == 16) return &farn::farn_stage_kernel<2, 16, QM>;
+    if (QM == kQuantFp8 && r == 6) return &farn::farn_stage_kernel<2, 6, kQuantFp8>;
   } else if (vpt == 4) {
-    if (r == 8) return &farn::farn_stage_kernel<4, 8, Q>;
-    if (r == 12) return &farn::farn_stage_kernel<4, 12, Q>;
-    if (r == 16) return &farn::farn_stage_kernel<4, 16, Q>;
-    if (Q && r == 6) return &farn::farn_stage_kernel<4, 6, true>;
+    if (r == 8) return &farn::farn_stage_kernel<4, 8, QM>;
+    if (r == 12) return &farn::farn_stage_kernel<4, 12, QM>;
+    if (r == 16) return &farn::farn_stage_kernel<4, 16, QM>;
+    if (QM == kQuantFp8 && r == 6) return &farn::farn_stage_kernel<4, 6, kQuantFp8>;
   }
   return nullptr;
 }
 
-// quant: the instantiation that also writes the FP8 output
-VecKernel pick_stage(int vpt, int r, bool quant = false) {
-  return quant ? pick_stage_q<true>(vpt, r) : pick_stage_q<false>(vpt, r);
+// qm: the instantiation that also writes the FP8 or the NVFP4 output
+VecKernel pick_stage(int vpt, int r, int qm = kQuantNone) {
+  return qm == kQuantFp8     ? pick_stage_q<kQuantFp8>(vpt, r)
+         : qm == kQuantNvfp4 ? pick_stage_q<kQuantNvfp4>(vpt, r)
+                             : pick_stage_q<kQuantNone>(vpt, r);
 }
 
 VecKernel pick_combine_stage(int vpt, int r) {
@@ -218,10 +224,12 @@ int choose_vpt(int64_t sv) {
 //      that give >= 320 threads per SM and fit registers and shared memory;
 //   2. else one CTA per SM, 2 then 4 vectors per thread;
 // each with the largest of 16 / 12 / 8 chunks in flight per thread that fits.
-// kind: 0 plain stage kernel, 1 with the FP8 output, 2 the staged MoE combine
+// kind: 0 plain stage kernel, 1 with the FP8 output, 2 the staged MoE
+// combine, 3 with the NVFP4 output
 bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T,
                int kind) {
   const bool quant = kind == 1;
+  const int qm = kind == 1 ? kQuantFp8 : (kind == 3 ? kQuantNvfp4 : kQuantNone);
   if (ctx->force_vpt > 0 && ctx->force_vpt != vpt) return false;
   if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
   const int64_t nt = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
@@ -235,7 +243,7 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
     if (ctx->stage_r > 0 && cand != ctx->stage_r) continue;
     if ((size_t)cand * vpt * nt * 16 <= budget) r = cand;
   }
-  if (!r || !(kind == 2 ? pick_combine_stage(vpt, r) : pick_stage(vpt, r, quant)))
+  if (!r || !(kind == 2 ? pick_combine_stage(vpt, r) : pick_stage(vpt, r, qm)))
     return false;
   pl->variant = kVariantStage;
   pl->pb = 2;
@@ -268,10 +276,12 @@ bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int ki
 }
 
 int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
-              bool quant = false) {
+              int qm = kQuantNone) {
   Plan pl;
   pl.pb = pb;
-  // The FP8 output is produced by every kernel but the TMA-staged one.
+  const bool quant = qm != kQuantNone;
+  // The FP8 and NVFP4 outputs are produced by every kernel but the
+  // TMA-staged one.
   if (quant && ctx->force_variant == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
@@ -288,7 +298,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
                   ctx->force_cluster == 0)) &&
-      make_stage_plan(ctx, T, H, &pl, quant ? 1 : 0)) {
+      make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
     *out = pl;
     return FARN_OK;
   }
@@ -308,10 +318,16 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
       // one CTA per row with every thread loading all ranks at once is as
       // fast and needs no cluster barrier.)
       const int cap = ctx->max_cluster < 8 ? ctx->max_cluster : 8;
-      while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64) cs *= 2;
+      // (The NVFP4 output pairs vectors 2m, 2m+1 inside a CTA: even slices.)
+      while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64 &&
+             (qm != kQuantNvfp4 || (hv / (cs * 2)) % 2 == 0))
+        cs *= 2;
     }
-    if (want == kVariantCluster && cs == 1 && ctx->max_cluster >= 2 && hv % 2 == 0) cs = 2;
+    if (want == kVariantCluster && cs == 1 && ctx->max_cluster >= 2 && hv % 2 == 0 &&
+        (qm != kQuantNvfp4 || hv % 4 == 0))
+      cs = 2;
     if (cs > ctx->max_cluster || hv % cs != 0) return FARN_ERR_UNSUPPORTED;
+    if (qm == kQuantNvfp4 && (hv / cs) % 2 != 0) return FARN_ERR_UNSUPPORTED;
     const int64_t sv = hv / cs;
     int vpt;
     if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
@@ -334,6 +350,44 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   // Grid limit: rows beyond one pass are looped over inside the kernel.
   const int64_t max_grid = (int64_t)0x7FFFFFFF / pl.cs * pl.cs;
   if (pl.grid > max_grid) pl.grid = max_grid;
+  *out = pl;
+  return FARN_OK;
+}
+
+// The MoE combine's kernel.  Long inputs (T >= the stage threshold): the
+// staged gather kernel, which keeps R chunks of gathered rows in flight per
+// thread (GB300, T = 4096, K = 8, H = 7168: 87.9 % of the copy bandwidth
+// against 81.3 % for one CTA per row, whose 128 registers per thread leave
+// two CTAs per SM).  Otherwise one CTA per row, every thread one vector of
+// each gathered row for few rows (all loads in flight at once), 4 vectors
+// otherwise; the generic kernel for odd shapes and alignments.
+// FARN_VARIANT=stage / row / generic force one of them.
+int make_moe_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
+  Plan pl;
+  pl.pb = 2; pl.cs = 1; pl.stages = 0; pl.stage_stride = 0; pl.smem = 0; pl.stage_r = 0;
+  const int64_t hv = H / 8;
+  const int want = ctx->force_variant;
+  if (want == kVariantCluster || want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
+  if (vec_ok && want != kVariantGeneric && want != kVariantRow &&
+      (want == kVariantStage || (ctx->stage && T >= ctx->stage_min_t)) &&
+      make_stage_plan(ctx, T, H, &pl, 2)) {
+    *out = pl;
+    return FARN_OK;
+  }
+  if (want == kVariantStage) return FARN_ERR_UNSUPPORTED;
+  int vpt = T < ctx->small_t ? (hv <= 512 ? 1 : (hv <= 1024 ? 2 : 4)) : choose_vpt(hv);
+  if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
+  int64_t threads = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
+  if (!vec_ok || threads > 512 || want == kVariantGeneric) {
+    pl.variant = kVariantGeneric;
+    pl.vpt = 1;
+    pl.threads = 256;
+  } else {
+    pl.variant = kVariantCombine;
+    pl.vpt = vpt;
+    pl.threads = (int)threads;
+  }
+  pl.grid = T < 0x7FFFFFFF ? T : 0x7FFFFFFF;
   *out = pl;
   return FARN_OK;
 }
@@ -372,15 +426,20 @@ const char* farn_status_string(int status) {
 namespace {
 
 // The argument checks for partials of `pb` bytes per element; with an FP8
-// output (q_out [T,H] bytes and scale_out [T] floats, both non-null)
-// norm_out may be null.
+// output (qm 1: q_out [T,H] bytes and scale_out [T] floats) or an NVFP4
+// output (qm 2: q_out [T,H/2] bytes and scale_out [T,H/16] bytes, H a
+// multiple of 16, tensor scale g finite and > 0), both non-null, norm_out
+// may be null.
 int check_args_pb(const void* const* partials, int W, int pb, const void* residual,
                   const void* weight, float eps, int64_t T, int64_t H,
                   const void* reduced_out, const void* residual_out, const void* norm_out,
                   const void* q_out = nullptr, const void* scale_out = nullptr,
-                  bool quant = false) {
+                  int qm = kQuantNone, float g = 1.0f) {
+  const bool quant = qm != kQuantNone;
   if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1) return FARN_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.0f) return FARN_ERR_INVALID_ARG;
+  if (qm == kQuantNvfp4 && (H % 16 != 0 || !isfinite(g) || !(g > 0.0f)))
+    return FARN_ERR_INVALID_ARG;
   if (H > INT64_MAX / 4 || (T > 0 && T > INT64_MAX / (4 * H))) return FARN_ERR_INVALID_ARG;
   // With no rows nothing is read or written: empty tensors may have null
   // data pointers.
@@ -393,7 +452,9 @@ int check_args_pb(const void* const* partials, int W, int pb, const void* residu
   const int64_t nb = T * H * 2, xb = T * H * pb, wb = H * 2;
   // outputs and their byte extents (a null norm_out extends over nothing)
   const void* outs[5] = {reduced_out, residual_out, norm_out, q_out, scale_out};
-  const int64_t ob[5] = {nb, nb, norm_out ? nb : 0, quant ? T * H : 0, quant ? T * 4 : 0};
+  const int64_t qb = qm == kQuantFp8 ? T * H : (qm == kQuantNvfp4 ? T * H / 2 : 0);
+  const int64_t sb = qm == kQuantFp8 ? T * 4 : (qm == kQuantNvfp4 ? T * H / 16 : 0);
+  const int64_t ob[5] = {nb, nb, norm_out ? nb : 0, qb, sb};
   for (int i = 0; i < 5; ++i) {
     for (int j = i + 1; j < 5; ++j)
       if (overlaps(outs[i], ob[i], outs[j], ob[j])) return FARN_ERR_ALIAS;
@@ -504,11 +565,14 @@ int farn_create(farn_ctx** out, int device) {
   }
   memset(c->stage_regs, 0, sizeof c->stage_regs);
   for (int vpt = 2; vpt <= 4; vpt *= 2) {
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 10; ++i) {
       // dynamic + static shared memory may not exceed the opt-in limit;
-      // i < 3: plain kernels, i >= 3: FP8-output kernels (depths 16..6)
+      // i < 3: plain kernels, 3..6: FP8-output kernels (depths 16..6),
+      // 7..9: NVFP4-output kernels
       cudaFuncAttributes fa;
-      const void* k = (const void*)pick_stage(vpt, kStageDepths[i < 3 ? i : i - 3], i >= 3);
+      const int qm = i < 3 ? kQuantNone : (i < 7 ? kQuantFp8 : kQuantNvfp4);
+      const int depth = kStageDepths[i < 3 ? i : (i < 7 ? i - 3 : i - 7)];
+      const void* k = (const void*)pick_stage(vpt, depth, qm);
       if (cudaFuncGetAttributes(&fa, k) != cudaSuccess ||
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                c->max_smem - (int)fa.sharedSizeBytes) != cudaSuccess) {
@@ -516,7 +580,7 @@ int farn_create(farn_ctx** out, int device) {
         cudaGetLastError();
         return FARN_ERR_CUDA;
       }
-      int& regs = c->stage_regs[i >= 3][vpt >= 4];
+      int& regs = c->stage_regs[qm == kQuantNone ? 0 : (qm == kQuantFp8 ? 1 : 3)][vpt >= 4];
       if (fa.numRegs > regs) regs = fa.numRegs;
     }
     for (int i = 0; i < 3; ++i) {       // the staged MoE combine
@@ -605,8 +669,13 @@ int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int flags, int W, in
                     const void* norm_out, int* variant, int* cluster_size, int* threads) {
   if (!ctx || !variant || !cluster_size || !threads) return FARN_ERR_INVALID_ARG;
   const int pb = dtype_bytes(partial_dtype);
-  if (!pb || (flags & ~FARN_PLAN_FP8_OUT)) return FARN_ERR_INVALID_ARG;
-  const bool quant = (flags & FARN_PLAN_FP8_OUT) != 0;
+  if (!pb || (flags & ~(FARN_PLAN_FP8_OUT | FARN_PLAN_NVFP4_OUT)) ||
+      flags == (FARN_PLAN_FP8_OUT | FARN_PLAN_NVFP4_OUT))
+    return FARN_ERR_INVALID_ARG;
+  const int qm = (flags & FARN_PLAN_FP8_OUT) ? kQuantFp8
+                 : (flags & FARN_PLAN_NVFP4_OUT) ? kQuantNvfp4 : kQuantNone;
+  const bool quant = qm != kQuantNone;
+  if (qm == kQuantNvfp4 && H % 16 != 0) return FARN_ERR_INVALID_ARG;
   // The choice depends on the shape, the dtype, the FP8 flag and the
   // pointers' alignment only; aliasing is not checked here.
   if (!partials || W < 1 || W > FARN_MAX_W || T < 0 || H < 1 || !residual || !weight ||
@@ -618,10 +687,28 @@ int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int flags, int W, in
   int st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out ? norm_out : reduced_out, H),
-                 pb, &pl, quant);
+                 pb, &pl, qm);
   if (st != FARN_OK) return st;
   *variant = pl.variant;
   *cluster_size = pl.cs;
+  *threads = pl.threads;
+  return FARN_OK;
+}
+
+int farn_plan_moe_combine(const farn_ctx* ctx, int K, int64_t T, int64_t H,
+                          const void* expert_out, const void* residual, const void* weight,
+                          const void* reduced_out, const void* residual_out,
+                          const void* norm_out, int* variant, int* threads) {
+  if (!ctx || !variant || !threads || K < 1 || K > FARN_MAX_W || T < 0 || H < 1 ||
+      !expert_out || !residual || !weight || !reduced_out || !residual_out || !norm_out)
+    return FARN_ERR_INVALID_ARG;
+  const bool vec_ok = H % 8 == 0 && aligned16(expert_out) && aligned16(residual) &&
+                      aligned16(weight) && aligned16(reduced_out) && aligned16(residual_out) &&
+                      aligned16(norm_out);
+  Plan pl;
+  const int st = make_moe_plan(ctx, T, H, vec_ok, &pl);
+  if (st != FARN_OK) return st;
+  *variant = pl.variant;
   *threads = pl.threads;
   return FARN_OK;
 }
@@ -634,17 +721,18 @@ int farn_forward(const farn_ctx* ctx, const void* const* partials, int W,
                             reduced_out, residual_out, norm_out, stream);
 }
 
-// farn_forward_typed and farn_forward_quant: q_out/scale_out and quant only
-// for the FP8 output.
+// farn_forward_typed, farn_forward_quant and farn_forward_nvfp4: q_out,
+// scale_out, qm and g only for a quantised copy of norm_out (FP8: scale_out
+// is float [T]; NVFP4: bytes [T,H/16], g the tensor scale).
 static int forward_impl(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
                         int W, const void* residual, const void* weight, float eps, int64_t T,
                         int64_t H, void* reduced_out, void* residual_out, void* norm_out,
-                        void* q_out, float* scale_out, bool quant, cudaStream_t stream) {
+                        void* q_out, void* scale_out, int qm, float g, cudaStream_t stream) {
   if (!ctx) return FARN_ERR_INVALID_ARG;
   const int pb = dtype_bytes(partial_dtype);
   if (!pb) return FARN_ERR_INVALID_ARG;
   int st = check_args_pb(partials, W, pb, residual, weight, eps, T, H, reduced_out,
-                         residual_out, norm_out, q_out, scale_out, quant);
+                         residual_out, norm_out, q_out, scale_out, qm, g);
   if (st != FARN_OK) return st;
   if (T == 0) return FARN_OK;
   if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
@@ -654,8 +742,9 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out ? norm_out : reduced_out, H) &&
-                     (!quant || ((uintptr_t)q_out & 15u) == 0),
-                 pb, &pl, quant);
+                     (qm != kQuantFp8 || ((uintptr_t)q_out & 15u) == 0) &&
+                     (qm != kQuantNvfp4 || ((uintptr_t)q_out & 3u) == 0),
+                 pb, &pl, qm);
   if (st != FARN_OK) return st;
 
   farn::Params prm;
@@ -666,8 +755,14 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   prm.reduced = reduced_out;
   prm.residual_out = residual_out;
   prm.norm_out = norm_out;
-  prm.q_out = static_cast<uint8_t*>(q_out);
-  prm.scale_out = scale_out;
+  if (qm == kQuantFp8) {
+    prm.q_out = static_cast<uint8_t*>(q_out);
+    prm.scale_out = static_cast<float*>(scale_out);
+  } else if (qm == kQuantNvfp4) {
+    prm.fp4_q = static_cast<uint8_t*>(q_out);
+    prm.fp4_s = static_cast<uint8_t*>(scale_out);
+    prm.fp4_g = g;
+  }
   prm.T = T;
   prm.H = H;
   prm.W = W;
@@ -676,8 +771,8 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   prm.stages = pl.stages;
   prm.stage_stride = pl.stage_stride;
 
-  DeviceGuard g(ctx->device);
-  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  DeviceGuard dg(ctx->device);
+  if (!dg.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
@@ -711,7 +806,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   } else if (pl.variant == kVariantBulk) {
     err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt), prm);
   } else if (pl.variant == kVariantStage) {
-    err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r, quant), prm);
+    err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r, qm), prm);
   } else {
     VecKernel k = pick_vec(pl.vpt, pl.cs, pb);
     err = cudaLaunchKernelEx(&cfg, k, prm);
@@ -728,7 +823,8 @@ int farn_forward_typed(const farn_ctx* ctx, const void* const* partials, int par
                        int64_t H, void* reduced_out, void* residual_out, void* norm_out,
                        cudaStream_t stream) {
   return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
-                      reduced_out, residual_out, norm_out, nullptr, nullptr, false, stream);
+                      reduced_out, residual_out, norm_out, nullptr, nullptr, kQuantNone, 1.0f,
+                      stream);
 }
 
 int farn_forward_quant(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
@@ -736,7 +832,17 @@ int farn_forward_quant(const farn_ctx* ctx, const void* const* partials, int par
                        int64_t H, void* reduced_out, void* residual_out, void* norm_out,
                        void* norm_q, float* row_scale, cudaStream_t stream) {
   return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
-                      reduced_out, residual_out, norm_out, norm_q, row_scale, true, stream);
+                      reduced_out, residual_out, norm_out, norm_q, row_scale, kQuantFp8, 1.0f,
+                      stream);
+}
+
+int farn_forward_nvfp4(const farn_ctx* ctx, const void* const* partials, int partial_dtype,
+                       int W, const void* residual, const void* weight, float eps, int64_t T,
+                       int64_t H, float tensor_scale, void* reduced_out, void* residual_out,
+                       void* norm_out, void* norm_fp4, void* block_scale, cudaStream_t stream) {
+  return forward_impl(ctx, partials, partial_dtype, W, residual, weight, eps, T, H,
+                      reduced_out, residual_out, norm_out, norm_fp4, block_scale, kQuantNvfp4,
+                      tensor_scale, stream);
 }
 
 // ------------------------------------------------------------------------
@@ -770,25 +876,14 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
     return FARN_ERR_CUDA;
 
-  // Kernel: one CTA per row, every thread one vector of each gathered row
-  // for few rows (all loads in flight at once), 4 vectors otherwise; the
-  // generic kernel for odd shapes and alignments.
-  const int64_t hv = H / 8;
   const bool vec_ok = H % 8 == 0 && aligned16(residual) && aligned16(weight) &&
                       aligned16(reduced_out) && aligned16(residual_out) &&
                       aligned16(norm_out) && (n_slots == 0 || aligned16(expert_out));
-  int vpt = T < ctx->small_t ? (hv <= 512 ? 1 : (hv <= 1024 ? 2 : 4)) : choose_vpt(hv);
-  if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
-  int64_t threads = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
-  const bool generic = !vec_ok || threads > 512 || ctx->force_variant == kVariantGeneric;
-  if (generic) threads = 256;
-  // The staged gather kernel on request only: on GB300 it measured no
-  // faster than the row kernel for the combine (80.1 % vs 81.4 % of the
-  // copy bandwidth at T = 4096, K = 8, H = 7168).
-  Plan spl;
-  const bool staged = !generic && ctx->force_variant == kVariantStage &&
-                      make_stage_plan(ctx, T, H, &spl, 2);
-  if (ctx->force_variant == kVariantStage && !staged) return FARN_ERR_UNSUPPORTED;
+  Plan pl;
+  const int st = make_moe_plan(ctx, T, H, vec_ok, &pl);
+  if (st != FARN_OK) return st;
+  const bool generic = pl.variant == kVariantGeneric;
+  const bool staged = pl.variant == kVariantStage;
   farn::Params prm;
   memset(&prm, 0, sizeof prm);
   prm.residual = residual;
@@ -808,10 +903,9 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   DeviceGuard g(ctx->device);
   if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
   cudaLaunchConfig_t cfg = {};
-  const int64_t grid = staged ? spl.grid : (T < 0x7FFFFFFF ? T : 0x7FFFFFFF);
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3((unsigned)(staged ? spl.threads : threads), 1, 1);
-  cfg.dynamicSmemBytes = staged ? spl.smem : 0;
+  cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+  cfg.dynamicSmemBytes = staged ? pl.smem : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -822,10 +916,10 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   if (generic) {
     err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel<2, true>, prm);
   } else if (staged) {
-    err = cudaLaunchKernelEx(&cfg, pick_combine_stage(spl.vpt, spl.stage_r), prm);
+    err = cudaLaunchKernelEx(&cfg, pick_combine_stage(pl.vpt, pl.stage_r), prm);
   } else {
-    VecKernel k = vpt == 1 ? &farn::farn_combine_kernel<1>
-                           : (vpt == 2 ? &farn::farn_combine_kernel<2> : &farn::farn_combine_kernel<4>);
+    VecKernel k = pl.vpt == 1 ? &farn::farn_combine_kernel<1>
+                  : (pl.vpt == 2 ? &farn::farn_combine_kernel<2> : &farn::farn_combine_kernel<4>);
     err = cudaLaunchKernelEx(&cfg, k, prm);
   }
   if (err != cudaSuccess) {

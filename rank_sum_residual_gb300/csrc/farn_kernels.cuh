@@ -48,6 +48,13 @@ struct Params {
   // bytes and scale_out [T] fp32, or null; norm_out may then be null too
   uint8_t* q_out;
   float* scale_out;
+  // optional NVFP4 output of norm_out (row, cluster, generic and stage
+  // kernels): fp4_q [T,H/2] bytes of E2M1 codes (element 2i in the low
+  // nibble), fp4_s [T,H/16] E4M3 block scales, fp4_g the tensor scale;
+  // H % 16 == 0.  Null when not wanted.
+  uint8_t* fp4_q;
+  uint8_t* fp4_s;
+  float fp4_g;
   // MoE combine only (farn_combine_kernel, farn_generic_kernel<2, true>):
   // W is K, the experts per token
   const void* expert_out;  // bf16 [n_slots, H]
@@ -95,6 +102,52 @@ __device__ __forceinline__ float e4m3_row_inv(float amax) {
   return amax > 0.0f ? 448.0f / amax : 1.0f;
 }
 
+// Two fp32 values to E2M1 (round to nearest even, finite saturation), lo in
+// bits 0-3 and hi in bits 4-7.  One cvt.rn.satfinite.e2m1x2.f32.
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The value of an E4M3 byte (exact: E4M3 -> f16 -> f32).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\t.reg .b32 x;\n\tcvt.rn.f16x2.e4m3x2 x, %1;\n\t"
+      "mov.b32 {lo, hi}, x;\n\tcvt.f32.f16 %0, lo;\n\t}" : "=f"(f) : "h"((uint16_t)b));
+  return f;
+}
+
+// NVFP4 codes of one 16-byte vector nv (8 bf16 values of norm_out) whose
+// 16-element block is completed by the vector of lane ^ 1; every lane of
+// the warp calls it.  Block amax (NaN ignored) -> E4M3 scale
+// s = E4M3((amax / 6) * g) -> inv = g / value(s) (IEEE divisions) ->
+// E2M1(x * inv) with magnitudes above 6 saturated (min(x, 6) also sends a
+// NaN to +6); a block whose scale is 0 gets all-zero codes.  Returns the 8
+// codes (element 2i in the low nibble of byte i); *sb gets the scale byte.
+__device__ __forceinline__ uint32_t nvfp4_vec(uint4 nv, float g, uint32_t* sb) {
+  const uint32_t n[4] = {nv.x, nv.y, nv.z, nv.w};
+  float mx = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fmaxf(fabsf(bf_lo(n[e])), fabsf(bf_hi(n[e]))));
+  mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  const uint32_t s = pack_e4m3x2((mx / 6.0f) * g, 0.0f) & 0xFFu;
+  const float sv = e4m3_to_f32(s);
+  const float inv = g / sv;
+  uint32_t word = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    word |= pack_e2m1x2(fminf(bf_lo(n[e]) * inv, 6.0f), fminf(bf_hi(n[e]) * inv, 6.0f))
+            << (8 * e);
+  *sb = s;
+  return sv > 0.0f ? word : 0u;
+}
+
+__device__ __forceinline__ void st_stream_u32(uint8_t* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -139,11 +192,17 @@ __device__ __forceinline__ void add8f(float* acc, uint4 a, uint4 b) {
   acc[6] += __uint_as_float(b.z); acc[7] += __uint_as_float(b.w);
 }
 
+// Eight bf16 values (one 16-byte vector) added in place.  The mixed-precision
+// add.rn.f32.bf16 widens its bf16 operand (exactly) and rounds the fp32 sum
+// once: the same addition as acc + bf_lo/bf_hi(v), one instruction per
+// element instead of an unpack and an add.
 __device__ __forceinline__ void add8(float* acc, uint4 v) {
-  acc[0] += bf_lo(v.x); acc[1] += bf_hi(v.x);
-  acc[2] += bf_lo(v.y); acc[3] += bf_hi(v.y);
-  acc[4] += bf_lo(v.z); acc[5] += bf_hi(v.z);
-  acc[6] += bf_lo(v.w); acc[7] += bf_hi(v.w);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(acc[2 * e]), "+f"(acc[2 * e + 1]) : "r"(w[e]));
 }
 
 // ---------------------------------------------------------------- cluster
@@ -199,7 +258,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // per 8 elements); residual, weight and outputs are bf16 either way.  At
 // most 512 threads per CTA (128 registers per thread).
 template <int VPT, int CS, int PB = 2>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, 1)
 farn_vec_kernel(const __grid_constant__ Params p) {
   constexpr int PV = PB / 2;
   constexpr int G = (8 / (VPT * PV)) > 0 ? (8 / (VPT * PV)) : 1;
@@ -402,6 +461,21 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       }
       if (tid == 0 && slice == 0) p.scale_out[row] = scale;
     }
+
+    if (p.fp4_q) {
+      // NVFP4 output: blocks of 16 elements are vector pairs (j, j ^ 1) of
+      // neighbouring lanes (the host keeps the slice's vector count even).
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * blockDim.x;
+        uint32_t sb;
+        const uint32_t codes = nvfp4_vec(nb[k], p.fp4_g, &sb);
+        if (j < sv) {
+          st_stream_u32(p.fp4_q + (base + j) * 4, codes);
+          if ((j & 1) == 0) p.fp4_s[(base + j) >> 1] = (uint8_t)sb;
+        }
+      }
+    }
   }
 }
 
@@ -489,6 +563,32 @@ farn_generic_kernel(const __grid_constant__ Params p) {
         p.q_out[off + h] = (uint8_t)(pack_e4m3x2(n * inv, 0.0f) & 0xFFu);
       }
       if (tid == 0) p.scale_out[row] = scale;
+    }
+    if (p.fp4_q) {
+      // NVFP4 output: a third pass, every lane on every step so that the
+      // 16 lanes of a block (blockDim.x is a multiple of 16, H % 16 == 0)
+      // reduce its amax and pair their codes by shuffles.
+      for (int64_t h0 = 0; h0 < p.H; h0 += blockDim.x) {
+        const int64_t h = h0 + tid;
+        const bool in = h < p.H;
+        float n = 0.0f;
+        if (in) {
+          const float q = __uint_as_float((uint32_t)ro_out[off + h] << 16);
+          const float w = __uint_as_float((uint32_t)wt[h] << 16);
+          n = __uint_as_float((uint32_t)to_bf16((q * rstd) * w) << 16);
+        }
+        float bmx = fmaxf(0.0f, fabsf(n));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) bmx = fmaxf(bmx, __shfl_xor_sync(0xFFFFFFFFu, bmx, o));
+        const uint32_t s = pack_e4m3x2((bmx / 6.0f) * p.fp4_g, 0.0f) & 0xFFu;
+        const float sv = e4m3_to_f32(s);
+        const float inv = p.fp4_g / sv;
+        uint32_t code = pack_e2m1x2(fminf(n * inv, 6.0f), 0.0f) & 0xFu;
+        if (!(sv > 0.0f)) code = 0;
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
+        if (in && (h & 1) == 0) p.fp4_q[(off + h) >> 1] = (uint8_t)(code | (other << 4));
+        if (in && (h & 15) == 0) p.fp4_s[(off + h) >> 4] = (uint8_t)s;
+      }
     }
   }
 }
@@ -926,10 +1026,10 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
-// QUANT: also write the FP8 copy of norm_out (p.q_out, p.scale_out; p.norm_out
-// may be null), as farn_vec_kernel does; compiled separately so the plain
-// kernel is unchanged.
-template <int VPT, int R, bool QUANT = false>
+// QM 1: also write the FP8 copy of norm_out (p.q_out, p.scale_out); QM 2:
+// the NVFP4 copy (p.fp4_q, p.fp4_s); p.norm_out may then be null.  Each is
+// compiled separately so the plain kernel is unchanged.
+template <int VPT, int R, int QM = 0>
 __global__ void __launch_bounds__(512)
 farn_stage_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -1064,7 +1164,7 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     ss = warp_sum(ss);
     float* ws = warp_ss[it & 1];
     if (lane == 0) ws[warp] = ss;
-    if constexpr (QUANT) {
+    if constexpr (QM == 1) {
       if (row_prev >= 0) {
         const float m = warp_max(mx_prev);
         if (lane == 0) warp_mx[(it - 1) & 1][warp] = m;
@@ -1073,7 +1173,7 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     __syncthreads();
     float tot = 0.0f;
     for (int w = 0; w < nwarps; ++w) tot += ws[w];
-    if constexpr (QUANT) {
+    if constexpr (QM == 1) {
       if (row_prev >= 0) {
         const float* wm = warp_mx[(it - 1) & 1];
         float amax = 0.0f;
@@ -1096,15 +1196,27 @@ farn_stage_kernel(const __grid_constant__ Params p) {
           const float n0 = (bf_lo(qv[e]) * rstd) * bf_lo(w[e]);
           const float n1 = (bf_hi(qv[e]) * rstd) * bf_hi(w[e]);
           n[e] = pack_bf16x2(n0, n1);
-          if constexpr (QUANT) mx = fmaxf(mx, fmaxf(fabsf(bf_lo(n[e])), fabsf(bf_hi(n[e]))));
+          if constexpr (QM == 1) mx = fmaxf(mx, fmaxf(fabsf(bf_lo(n[e])), fabsf(bf_hi(n[e]))));
         }
-        if constexpr (QUANT) nb[k] = make_uint4(n[0], n[1], n[2], n[3]);
-        if (!QUANT || p.norm_out)
+        if constexpr (QM != 0) nb[k] = make_uint4(n[0], n[1], n[2], n[3]);
+        if (QM == 0 || p.norm_out)
           st_stream(reinterpret_cast<uint4*>(p.norm_out) + base + j,
                     make_uint4(n[0], n[1], n[2], n[3]));
       }
     }
-    if constexpr (QUANT) {
+    if constexpr (QM == 2) {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * nt;
+        uint32_t sb;
+        const uint32_t codes = nvfp4_vec(j < hv ? nb[k] : make_uint4(0u, 0u, 0u, 0u), p.fp4_g, &sb);
+        if (j < hv) {
+          st_stream_u32(p.fp4_q + (base + j) * 4, codes);
+          if ((j & 1) == 0) p.fp4_s[(base + j) >> 1] = (uint8_t)sb;
+        }
+      }
+    }
+    if constexpr (QM == 1) {
       // the row's amax (exact, NaN ignored) is reduced at the next row's
       // barrier, or after the loop for the last row
 #pragma unroll
@@ -1113,7 +1225,7 @@ farn_stage_kernel(const __grid_constant__ Params p) {
       row_prev = row;
     }
   }
-  if constexpr (QUANT) {
+  if constexpr (QM == 1) {
     if (row_prev >= 0) {
       const float m = warp_max(mx_prev);
       if (lane == 0) warp_mx[(it - 1) & 1][warp] = m;
@@ -1132,10 +1244,13 @@ farn_stage_kernel(const __grid_constant__ Params p) {
 // persistent CTA walks its rows; the chunks of a row are its K gathered
 // expert rows (expert_out[index[t,k]]) and then its residual row; every
 // thread keeps R chunks of its own 16-byte vectors in flight with
-// cp.async.  The issuing thread reads the slot index through L1 when it
-// issues a chunk (a skipped slot issues no copy, only an empty group); the
-// consumer reads the same index and the gate, and adds gate * x with the
-// product and the sum each rounded (no fused multiply-add), k in order.
+// cp.async.  A row's routing (K <= 32 slots and gates) lives in registers
+// across the warp, lane k holding column k, and __shfl_sync hands column c
+// to every lane; the issuing side and the consuming side each load it one
+// of the CTA's rows ahead of use, so no chunk waits on an index load.  A
+// slot outside [0, n_slots) issues no copy (only an empty group) and adds
+// nothing; the consumer adds gate * x with the product and the sum each
+// rounded (no fused multiply-add), k in order.
 template <int VPT, int R>
 __global__ void __launch_bounds__(512)
 farn_combine_stage_kernel(const __grid_constant__ Params p) {
@@ -1146,6 +1261,7 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
   const int nwarps = (nt + 31) >> 5;
   const int64_t hv = p.H >> 3;
   const int K = p.W;
+  const int64_t step = gridDim.x;
   const float Hf = (float)p.H;
   __shared__ float warp_ss[2][32];
   const uint32_t slots = (uint32_t)__cvta_generic_to_shared(smem);
@@ -1153,10 +1269,14 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
   auto slot_addr = [&](int s, int k) -> uint32_t {
     return slots + (uint32_t)(((s * VPT + k) * nt + tid) * 16);
   };
-  auto slot_of = [&](int64_t row, int c) -> int32_t {
-    const int32_t sl = __ldg(p.index + row * K + c);
-    return (sl >= 0 && (int64_t)sl < p.n_slots) ? sl : -1;
+  // Routing column `lane` of row r (-1 / 0 past the last row or column).
+  auto load_slot = [&](int64_t r) -> int32_t {
+    return (r < p.T && lane < K) ? __ldg(p.index + r * K + lane) : -1;
   };
+  auto load_gate = [&](int64_t r) -> float {
+    return (r < p.T && lane < K) ? __ldg(p.gates + r * K + lane) : 0.0f;
+  };
+  auto valid = [&](int32_t sl) { return sl >= 0 && (int64_t)sl < p.n_slots; };
 
   pdl_wait();
   uint4 wv[VPT];
@@ -1168,27 +1288,32 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
 
   int64_t irow = blockIdx.x;
   int ic = 0;
+  int32_t i_cur = load_slot(irow), i_nxt = load_slot(irow + step);
+  // consumer's routing: this row (c_*) and the CTA's next row (n_*)
+  int32_t c_sl = i_cur, n_sl = i_nxt;
+  float c_gt = load_gate(irow), n_gt = load_gate(irow + step);
   auto issue_next = [&](int s) {
-    if (irow < p.T) {
+    if (irow < p.T) {                       // uniform across the CTA
+      const uint4* src = nullptr;
       if (ic < K) {
-        const int32_t sl = slot_of(irow, ic);
-        if (sl >= 0) {
-          const uint4* src = ex4 + (int64_t)sl * hv;
-#pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            const int j = tid + k * nt;
-            if (j < hv) cp_async16(slot_addr(s, k), src + j);
-          }
-        }
+        const int32_t sl = __shfl_sync(0xFFFFFFFFu, i_cur, ic);
+        if (valid(sl)) src = ex4 + (int64_t)sl * hv;
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(p.residual) + irow * hv;
+        src = reinterpret_cast<const uint4*>(p.residual) + irow * hv;
+      }
+      if (src) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           const int j = tid + k * nt;
           if (j < hv) cp_async16(slot_addr(s, k), src + j);
         }
       }
-      if (++ic > K) { ic = 0; irow += gridDim.x; }
+      if (++ic > K) {
+        ic = 0;
+        irow += step;
+        i_cur = i_nxt;
+        i_nxt = load_slot(irow + step);
+      }
     }
     cp_async_commit();
   };
@@ -1196,18 +1321,8 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
   for (int s = 0; s < R; ++s) issue_next(s);
 
   int q = 0, it = 0, res_slot = 0;
-  for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
+  for (int64_t row = blockIdx.x; row < p.T; row += step, ++it) {
     const int64_t base = row * hv;
-    // The issue cursor is about a row ahead: fetch the index and gate rows
-    // of the next two rows into L1 now, so issuing their chunks does not
-    // wait on an L2 miss.
-    if (tid < 2) {
-      const int64_t nr = row + (int64_t)(tid + 1) * gridDim.x;
-      if (nr < p.T) {
-        asm volatile("prefetch.global.L1 [%0];" :: "l"(p.index + nr * K));
-        asm volatile("prefetch.global.L1 [%0];" :: "l"(p.gates + nr * K));
-      }
-    }
     float acc[VPT][8];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
@@ -1218,9 +1333,9 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
       const int s = q % R;
       cp_async_wait<R - 1>();
       if (c < K) {
-        const int32_t sl = slot_of(row, c);
-        if (sl >= 0) {
-          const float gt = __ldg(p.gates + row * K + c);
+        const int32_t sl = __shfl_sync(0xFFFFFFFFu, c_sl, c);
+        const float gt = __shfl_sync(0xFFFFFFFFu, c_gt, c);
+        if (valid(sl)) {
 #pragma unroll
           for (int k = 0; k < VPT; ++k) {
             const int j = tid + k * nt;
@@ -1246,7 +1361,12 @@ farn_combine_stage_kernel(const __grid_constant__ Params p) {
         res_slot = s;
       }
     }
-    if (row + gridDim.x >= p.T) pdl_trigger();
+    // the next row's routing is in registers; fetch the one after it
+    c_sl = n_sl;
+    c_gt = n_gt;
+    n_sl = load_slot(row + 2 * step);
+    n_gt = load_gate(row + 2 * step);
+    if (row + step >= p.T) pdl_trigger();
 
     uint4 ro[VPT];
     float ss = 0.0f;

@@ -72,6 +72,8 @@ class Problem:
     weight: Dist = Dist(NORMAL, 1.0, 0.1)
     partial_dtype: str = "bf16"      # or "f32"
     fp8_out: bool = False            # also write norm_out as E4M3 + row scales
+    nvfp4_out: bool = False          # also write norm_out as NVFP4 + block scales
+    tensor_scale: float = 1.0        # the NVFP4 tensor scale
     norm_out: bool = True            # write the bf16 norm_out
     kind: str = "rank_sum"           # or "moe_combine" (W = experts per token)
 
@@ -90,10 +92,12 @@ class Problem:
 
     def write_bytes(self) -> int:
         """reduced and residual_out (T*H*2 each), norm_out (T*H*2) if
-        written, and with the FP8 output T*H bytes plus T*4 of scales."""
+        written, with the FP8 output T*H bytes plus T*4 of scales, with the
+        NVFP4 output T*H/2 bytes of codes plus T*H/16 of block scales."""
         n = self.T * self.H
         return 2 * n * 2 + (n * 2 if self.norm_out else 0) + \
-            ((n + 4 * self.T) if self.fp8_out else 0)
+            ((n + 4 * self.T) if self.fp8_out else 0) + \
+            ((n // 2 + n // 16) if self.nvfp4_out else 0)
 
     def algorithmic_bytes(self) -> int:
         return self.read_bytes() + self.write_bytes()
@@ -134,6 +138,13 @@ WORKLOADS = {
     "prefill_fp8": [Problem("prefill_fp8", 8, 8192, 8192, 1e-6, 0,
                             Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
                             N01, Dist(UNIFORM, 0.5, 1.5), fp8_out=True, norm_out=False)],
+    # the prefill shape writing norm_out as NVFP4 (E2M1 codes, E4M3 scales
+    # per 16 elements) instead of bf16; the tensor scale maps an amax of 16
+    # to the top of the E4M3 x E2M1 range (448 * 6 / 16)
+    "prefill_nvfp4": [Problem("prefill_nvfp4", 8, 8192, 8192, 1e-6, 0,
+                              Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),
+                              N01, Dist(UNIFORM, 0.5, 1.5), nvfp4_out=True, norm_out=False,
+                              tensor_scale=168.0)],
     # the prefill shape with fp32 partials (e.g. straight from GEMM epilogues)
     "prefill_f32": [Problem("prefill_f32", 8, 8192, 8192, 1e-6, 0,
                             Dist(NORMAL, 0.0, 0.5, 0.001, 50.0),

@@ -82,6 +82,7 @@ def test_algorithmic_bytes_formula(name):
         if p.kind == "moe_combine":           # + int32 index and fp32 gate per slot
             read += p.T * p.W * 8
         write = (2 + p.norm_out) * p.T * p.H * 2 + (p.T * p.H + 4 * p.T) * p.fp8_out
+        write += (p.T * p.H // 2 + p.T * p.H // 16) * p.nvfp4_out   # codes + block scales
         assert p.algorithmic_bytes() == read + write
         assert bench.call_bytes(p, p.T) == read + write
 

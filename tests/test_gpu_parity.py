@@ -866,6 +866,38 @@ def test_moe_combine_mid_size(O, dev, variant):
         ctx.close()
 
 
+def test_moe_combine_plan(dev):
+    """Long inputs take the staged gather kernel, shorter ones one CTA per
+    row, odd alignments the generic kernel; FARN_VARIANT forces each."""
+    c = farn._context_for(0)
+    for T, want in ((4096, "stage"), (2048, "stage"), (2047, "combine"), (1, "combine")):
+        p = _moe(T, 8, 7168)
+        (ex, index, gates), res, w = synth.device_inputs(p, dev)
+        outs = [torch.empty_like(res) for _ in range(3)]
+        v, thr = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr(), res.data_ptr(),
+                                            w.data_ptr(), *[o.data_ptr() for o in outs])
+        assert v == want, (T, v)
+        assert 32 <= thr <= 512
+        if T == 4096:
+            v, _ = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr() + 2,
+                                              res.data_ptr(), w.data_ptr(),
+                                              *[o.data_ptr() for o in outs])
+            assert v == "generic"
+            for env, want_v in ((dict(FARN_VARIANT="row"), "combine"),
+                                (dict(FARN_VARIANT="generic"), "generic"),
+                                (dict(FARN_STAGE=0), "combine")):
+                ctx = make_ctx(**env)
+                try:
+                    v, _ = farn.farn_plan_moe_combine(ctx.handle, 8, T, p.H, ex.data_ptr(),
+                                                      res.data_ptr(), w.data_ptr(),
+                                                      *[o.data_ptr() for o in outs])
+                    assert v == want_v, (env, v)
+                finally:
+                    ctx.close()
+        del ex, index, gates, res, w, outs
+    torch.cuda.empty_cache()
+
+
 def test_moe_combine_unit_gates_match_forward(O, dev):
     """Gates of 1 and the slot layout of stacked partials: the combine and
     the rank-sum kernel give the same bits."""
