@@ -45,7 +45,8 @@ struct farn_ctx {
   int stage;           // 1: the cp.async-staged kernel serves long inputs
   int stage_r;         // 0 = choose; else chunks in flight per thread (8/12/16)
   int stage_ctas;      // 0 = choose; else resident stage CTAs per SM (1..4)
-  int64_t stage_min_t; // the stage kernel serves calls with at least this many rows
+  int64_t stage_min_t; // the stage kernel serves calls with at least this many rows,
+  int64_t stage_min_bytes;  // or half as many that read at least this many bytes
   int stage_regs[4][2];  // registers per thread of the staged kernels
                          // [plain, FP8, MoE combine, NVFP4][4 vectors]
   int max_smem;        // opt-in shared memory per CTA, bytes
@@ -57,8 +58,8 @@ namespace {
 typedef void (*VecKernel)(const farn::Params);
 
 // Chunks in flight per thread that the stage kernels are built for (the
-// FP8-output kernels also at 6, so that two of their CTAs share an SM at
-// H = 8192).
+// FP8- and NVFP4-output kernels also at 6, so that two of their CTAs share
+// an SM at H = 8192).
 constexpr int kStageDepths[4] = {16, 12, 8, 6};
 
 // Quantised copy of norm_out written alongside (the stage kernel's QM).
@@ -70,12 +71,14 @@ VecKernel pick_stage_q(int vpt, int r) {
     if (r == 8) return &farn::farn_stage_kernel<2, 8, QM>;
     if (r == 12) return &farn::farn_stage_kernel<2, 12, QM>;
     if (r == 16) return &farn::farn_stage_kernel<2, 16, QM>;
-    if (QM == kQuantFp8 && r == 6) return &farn::farn_stage_kernel<2, 6, kQuantFp8>;
+    if constexpr (QM != kQuantNone)
+      if (r == 6) return &farn::farn_stage_kernel<2, 6, QM>;
   } else if (vpt == 4) {
     if (r == 8) return &farn::farn_stage_kernel<4, 8, QM>;
     if (r == 12) return &farn::farn_stage_kernel<4, 12, QM>;
     if (r == 16) return &farn::farn_stage_kernel<4, 16, QM>;
-    if (QM == kQuantFp8 && r == 6) return &farn::farn_stage_kernel<4, 6, kQuantFp8>;
+    if constexpr (QM != kQuantNone)
+      if (r == 6) return &farn::farn_stage_kernel<4, 6, QM>;
   }
   return nullptr;
 }
@@ -220,15 +223,17 @@ int choose_vpt(int64_t sv) {
 // H = 2048 / 4096 at T = 1k-8k): what matters is both the bytes each SM
 // keeps in flight and having at least two CTAs (or one of 512 threads) per
 // SM, so that one row's reduction overlaps another row's loads.  So:
-//   1. 4, then 2 vectors per thread, with the fewest CTAs per SM (2..4)
-//      that give >= 320 threads per SM and fit registers and shared memory;
+//   1. 4, then 2 vectors per thread (2 first for the NVFP4 output), with the
+//      fewest CTAs per SM (2..4) that give >= 320 threads per SM and fit
+//      registers and shared memory;
 //   2. else one CTA per SM, 2 then 4 vectors per thread;
-// each with the largest of 16 / 12 / 8 chunks in flight per thread that fits.
+// each with the largest of 16 / 12 / 8 chunks in flight per thread that fits
+// (also 6 for the FP8 and NVFP4 outputs).
 // kind: 0 plain stage kernel, 1 with the FP8 output, 2 the staged MoE
 // combine, 3 with the NVFP4 output
 bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int64_t T,
                int kind) {
-  const bool quant = kind == 1;
+  const bool quant = kind == 1 || kind == 3;
   const int qm = kind == 1 ? kQuantFp8 : (kind == 3 ? kQuantNvfp4 : kQuantNone);
   if (ctx->force_vpt > 0 && ctx->force_vpt != vpt) return false;
   if (ctx->stage_ctas > 0 && ctx->stage_ctas != ctas) return false;
@@ -257,10 +262,23 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
   return true;
 }
 
+// Long enough for the persistent stage kernels: at least stage_min_t rows,
+// or half that many when the call reads at least stage_min_bytes.  (GB300,
+// T = 1024: the stage kernel 90.8 % / 85.0 % of the copy bandwidth against
+// 82.0 % / 80.8 % for the row kernel on the prefill / wide shapes, which
+// read 151 / 250 MB; 66.8 % against 71.1 % on nonpow2, 52 MB; at T = 512
+// the row kernel is ahead on all three.)
+bool long_call(const farn_ctx* ctx, int64_t T, int64_t in_bytes) {
+  return T >= ctx->stage_min_t || (T >= ctx->stage_min_t / 2 && in_bytes >= ctx->stage_min_bytes);
+}
+
 // bf16 partials only (fp32 partials take the row kernel, see the kernel).
 bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int kind) {
   const int64_t hv = H / 8;
-  const int vpts[2] = {4, 2};
+  // The NVFP4 kernel tries 2 vectors per thread first: at H = 8192 two CTAs
+  // of 512 threads (6 chunks in flight) measured 100.7 % of the copy
+  // bandwidth against 94.9 % for two CTAs of 256 threads at 4 vectors.
+  const int vpts[2] = {kind == 3 ? 2 : 4, kind == 3 ? 4 : 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
     return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, kind) ||
            stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T, kind);
@@ -275,8 +293,9 @@ bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int ki
   return stage_fit(ctx, hv, 2, 1, pl, T, kind) || stage_fit(ctx, hv, 4, 1, pl, T, kind);
 }
 
+// in_bytes: the bytes the call reads (partials, residual, weight).
 int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
-              int qm = kQuantNone) {
+              int qm, int64_t in_bytes) {
   Plan pl;
   pl.pb = pb;
   const bool quant = qm != kQuantNone;
@@ -296,7 +315,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   pl.stage_r = 0;
   if (vec_ok && pb == 2 && (want == kVariantStage ||
-                 (want == kVariantAuto && ctx->stage && T >= ctx->stage_min_t &&
+                 (want == kVariantAuto && ctx->stage && long_call(ctx, T, in_bytes) &&
                   ctx->force_cluster == 0)) &&
       make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
     *out = pl;
@@ -362,14 +381,14 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
 // each gathered row for few rows (all loads in flight at once), 4 vectors
 // otherwise; the generic kernel for odd shapes and alignments.
 // FARN_VARIANT=stage / row / generic force one of them.
-int make_moe_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, Plan* out) {
+int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   pl.pb = 2; pl.cs = 1; pl.stages = 0; pl.stage_stride = 0; pl.smem = 0; pl.stage_r = 0;
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
   if (want == kVariantCluster || want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   if (vec_ok && want != kVariantGeneric && want != kVariantRow &&
-      (want == kVariantStage || (ctx->stage && T >= ctx->stage_min_t)) &&
+      (want == kVariantStage || (ctx->stage && long_call(ctx, T, (int64_t)(K + 1) * T * H * 2))) &&
       make_stage_plan(ctx, T, H, &pl, 2)) {
     *out = pl;
     return FARN_OK;
@@ -544,6 +563,7 @@ int farn_create(farn_ctx** out, int device) {
   c->stage_ctas = env_int("FARN_STAGE_CTAS", 0);
   if (c->stage_ctas < 1 || c->stage_ctas > 4) c->stage_ctas = 0;
   c->stage_min_t = env_int("FARN_STAGE_MIN_T", 2048);
+  c->stage_min_bytes = (int64_t)env_int("FARN_STAGE_MIN_MB", 128) << 20;
   c->bulk = env_int("FARN_BULK", 0) != 0;
   c->bulk_ctas = env_int("FARN_BULK_CTAS", 1) == 2 ? 2 : 1;
   c->max_smem = 0;
@@ -565,10 +585,10 @@ int farn_create(farn_ctx** out, int device) {
   }
   memset(c->stage_regs, 0, sizeof c->stage_regs);
   for (int vpt = 2; vpt <= 4; vpt *= 2) {
-    for (int i = 0; i < 10; ++i) {
+    for (int i = 0; i < 11; ++i) {
       // dynamic + static shared memory may not exceed the opt-in limit;
       // i < 3: plain kernels, 3..6: FP8-output kernels (depths 16..6),
-      // 7..9: NVFP4-output kernels
+      // 7..10: NVFP4-output kernels (depths 16..6)
       cudaFuncAttributes fa;
       const int qm = i < 3 ? kQuantNone : (i < 7 ? kQuantFp8 : kQuantNvfp4);
       const int depth = kStageDepths[i < 3 ? i : (i < 7 ? i - 3 : i - 7)];
@@ -687,7 +707,7 @@ int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int flags, int W, in
   int st = make_plan(ctx, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out ? norm_out : reduced_out, H),
-                 pb, &pl, qm);
+                 pb, &pl, qm, (int64_t)W * T * H * pb + T * H * 2);
   if (st != FARN_OK) return st;
   *variant = pl.variant;
   *cluster_size = pl.cs;
@@ -706,7 +726,7 @@ int farn_plan_moe_combine(const farn_ctx* ctx, int K, int64_t T, int64_t H,
                       aligned16(weight) && aligned16(reduced_out) && aligned16(residual_out) &&
                       aligned16(norm_out);
   Plan pl;
-  const int st = make_moe_plan(ctx, T, H, vec_ok, &pl);
+  const int st = make_moe_plan(ctx, K, T, H, vec_ok, &pl);
   if (st != FARN_OK) return st;
   *variant = pl.variant;
   *threads = pl.threads;
@@ -744,7 +764,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
                                 norm_out ? norm_out : reduced_out, H) &&
                      (qm != kQuantFp8 || ((uintptr_t)q_out & 15u) == 0) &&
                      (qm != kQuantNvfp4 || ((uintptr_t)q_out & 3u) == 0),
-                 pb, &pl, qm);
+                 pb, &pl, qm, (int64_t)W * T * H * pb + T * H * 2);
   if (st != FARN_OK) return st;
 
   farn::Params prm;
@@ -880,7 +900,7 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
                       aligned16(reduced_out) && aligned16(residual_out) &&
                       aligned16(norm_out) && (n_slots == 0 || aligned16(expert_out));
   Plan pl;
-  const int st = make_moe_plan(ctx, T, H, vec_ok, &pl);
+  const int st = make_moe_plan(ctx, K, T, H, vec_ok, &pl);
   if (st != FARN_OK) return st;
   const bool generic = pl.variant == kVariantGeneric;
   const bool staged = pl.variant == kVariantStage;

@@ -249,6 +249,10 @@ def test_plan_choices(dev):
         assert plan(8, 8192, 8192) == ("stage", 1, 512)  # 2 vectors/thread, 1 CTA/SM
         assert plan(16, 4096, 7168) == ("stage", 1, 224)  # 4 vectors/thread, 2 CTAs/SM
         assert plan(4, 32768, 5120) == ("stage", 1, 160)
+        # half the row threshold when the call reads >= 128 MiB
+        assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
+        assert plan(8, 1023, 8192)[0] == "row"
+        assert plan(4, 1024, 5120)[0] == "row"          # 52 MB
         assert plan(8, 1, 4096)[0] == "cluster"
         assert plan(8, 1, 4096)[1] == 8
         assert plan(8, 64, 4096) == ("row", 1, 512)     # decode: all ranks at once
@@ -870,7 +874,9 @@ def test_moe_combine_plan(dev):
     """Long inputs take the staged gather kernel, shorter ones one CTA per
     row, odd alignments the generic kernel; FARN_VARIANT forces each."""
     c = farn._context_for(0)
-    for T, want in ((4096, "stage"), (2048, "stage"), (2047, "combine"), (1, "combine")):
+    # staged from 2048 rows, or from 1024 rows reading >= 128 MiB
+    for T, want in ((4096, "stage"), (2047, "stage"), (1100, "stage"), (1000, "combine"),
+                    (1, "combine")):
         p = _moe(T, 8, 7168)
         (ex, index, gates), res, w = synth.device_inputs(p, dev)
         outs = [torch.empty_like(res) for _ in range(3)]
