@@ -223,9 +223,9 @@ int choose_vpt(int64_t sv) {
 // H = 2048 / 4096 at T = 1k-8k): what matters is both the bytes each SM
 // keeps in flight and having at least two CTAs (or one of 512 threads) per
 // SM, so that one row's reduction overlaps another row's loads.  So:
-//   1. 4, then 2 vectors per thread (2 first for the NVFP4 output), with the
-//      fewest CTAs per SM (2..4) that give >= 320 threads per SM and fit
-//      registers and shared memory;
+//   1. 4, then 2 vectors per thread (2 first for the FP8 and NVFP4
+//      outputs), with the fewest CTAs per SM (2..4) that give >= 320
+//      threads per SM and fit registers and shared memory;
 //   2. else one CTA per SM, 2 then 4 vectors per thread;
 // each with the largest of 16 / 12 / 8 chunks in flight per thread that fits
 // (also 6 for the FP8 and NVFP4 outputs).
@@ -275,10 +275,13 @@ bool long_call(const farn_ctx* ctx, int64_t T, int64_t in_bytes) {
 // bf16 partials only (fp32 partials take the row kernel, see the kernel).
 bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int kind) {
   const int64_t hv = H / 8;
-  // The NVFP4 kernel tries 2 vectors per thread first: at H = 8192 two CTAs
-  // of 512 threads (6 chunks in flight) measured 100.7 % of the copy
-  // bandwidth against 94.9 % for two CTAs of 256 threads at 4 vectors.
-  const int vpts[2] = {kind == 3 ? 2 : 4, kind == 3 ? 4 : 2};
+  // The quantising kernels try 2 vectors per thread first: at H = 8192 two
+  // CTAs of 512 threads (6 chunks in flight) measured 101.0 % (NVFP4) and
+  // 95.1 % (FP8) of the copy bandwidth against 96.4 % and 94.8 % for two
+  // CTAs of 256 threads at 4 vectors.  (The staged MoE combine measured
+  // the other way: 86.1 % at 2 vectors x 448 threads, 89.1 % at 4 x 224.)
+  const bool two_first = kind == 1 || kind == 3;
+  const int vpts[2] = {two_first ? 2 : 4, two_first ? 4 : 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
     return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, kind) ||
            stage_fit(ctx, hv, vpts[1], ctx->stage_ctas, pl, T, kind);

@@ -1055,8 +1055,10 @@ __device__ __forceinline__ void cp_async_wait() {
 // QM 1: also write the FP8 copy of norm_out (p.q_out, p.scale_out); QM 2:
 // the NVFP4 copy (p.fp4_q, p.fp4_s); p.norm_out may then be null.  Each is
 // compiled separately so the plain kernel is unchanged.
+// The quantising kernels at 2 vectors per thread are built for two CTAs of
+// 512 threads per SM (at most 64 registers per thread).
 template <int VPT, int R, int QM = 0>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, (VPT == 2 && QM != 0) ? 2 : 0)
 farn_stage_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
