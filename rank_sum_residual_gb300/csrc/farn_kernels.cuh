@@ -210,8 +210,9 @@ __device__ __forceinline__ void add8(float* acc, uint4 v) {
 // addition, so the sums are those of add8).  Measured on GB300, the plain
 // stage kernel streams faster with this form (nonpow2 99.8 % vs 89 % of
 // the copy bandwidth, prefill 103.6 % vs 99.4 %), the quantising stage
-// kernels and the latency-bound row kernels with add8 (FP8 94.6 % vs
-// 91.5 %, NVFP4 92.3 % vs 90.3 %).
+// kernels, the TMA-staged kernel and the latency-bound row kernels with
+// add8 (FP8 94.6 % vs 91.5 %, NVFP4 92.3 % vs 90.3 %, bulk at nonpow2
+// 98.9 % vs 94.3 %).
 __device__ __forceinline__ void add8_x2(float* acc, uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -226,9 +227,9 @@ __device__ __forceinline__ void add8_x2(float* acc, uint4 v) {
 
 // acc[0..8) += g * f(v) for the eight bf16 values of one 16-byte vector,
 // the product and the sum each rounded to fp32 (__fmul_rn / __fadd_rn are
-// never fused into a multiply-add).  (A packed mul.rn.f32x2 / add.rn.f32x2
-// form was measured no faster and did not keep the product and the sum
-// separately rounded: it was dropped.)
+// never fused into a multiply-add).  Measured alternatives: packed
+// mul.rn.f32x2 / add.rn.f32x2 did not keep the products separately
+// rounded; scalar products with packed sums were exact but no faster.
 __device__ __forceinline__ void gate_add8(float* acc, float g, uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

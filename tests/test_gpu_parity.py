@@ -662,6 +662,54 @@ def test_cuda_graph_capture_and_replay(O, dev, name, T):
                       f"graph replay {k} {name} T={T}")
 
 
+def test_cuda_graph_quantised_and_moe(O, dev):
+    """The NVFP4 and FP8 outputs and the staged MoE combine captured in one
+    CUDA graph, replayed twice: the same bytes as eager calls."""
+    p = synth.workload("prefill")[0].with_T(2100)
+    xs, res, w = synth.device_inputs(p, dev)
+    pm = _moe(2100, 8, 2048, seed=21)
+    (ex, index, gates), mres, mw = synth.device_inputs(pm, dev)
+    eager = [farn.forward_nvfp4(xs, res, w, p.eps, 168.0), farn.forward_quant(xs, res, w, p.eps),
+             farn.moe_combine(ex, index, gates, mres, mw, pm.eps)]
+    torch.cuda.synchronize()
+    outs4 = tuple(torch.empty_like(t) for t in eager[0])
+    outs8 = tuple(torch.empty_like(t) for t in eager[1])
+    outsm = tuple(torch.empty_like(t) for t in eager[2])
+    c = farn._context_for(0)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    ptrs = [x.data_ptr() for x in xs]
+    with torch.cuda.graph(g, stream=s):
+        assert farn.farn_forward_nvfp4(c.handle, ptrs, farn.FARN_BF16, p.W, res.data_ptr(),
+                                       w.data_ptr(), p.eps, p.T, p.H, 168.0,
+                                       *[t.data_ptr() for t in outs4], s.cuda_stream) == 0
+        assert farn.farn_forward_quant(c.handle, ptrs, farn.FARN_BF16, p.W, res.data_ptr(),
+                                       w.data_ptr(), p.eps, p.T, p.H,
+                                       *[t.data_ptr() for t in outs8], s.cuda_stream) == 0
+        farn.moe_combine(ex, index, gates, mres, mw, pm.eps, out=outsm, stream=s)
+    for k in range(2):
+        for t in outs4 + outs8 + outsm:
+            t.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((outs4, outs8, outsm), eager):
+            for a, b in zip(got, want):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"replay {k}"
+
+
+@pytest.mark.parametrize("variant", ["auto", "stage", "row"])
+def test_moe_combine_32_experts(O, dev, variant):
+    """K = 32 (every lane of the routing registers in use), many rows per
+    persistent CTA."""
+    ctx = make_ctx(FARN_VARIANT=variant) if variant != "auto" else None
+    try:
+        _run_moe(O, dev, _moe(700, 32, 1024, seed=17), ctx=ctx, what=f"moe K=32 {variant}")
+    finally:
+        if ctx is not None:
+            ctx.close()
+
+
 def test_two_streams_concurrently(O, dev):
     """Independent calls on two streams at once (one long, one decode-sized)."""
     pa = synth.workload("prefill")[0].with_T(4096)
