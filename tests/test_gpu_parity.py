@@ -20,6 +20,7 @@ import oracle  # noqa: E402
 import rank_sum_residual_gb300 as farn  # noqa: E402
 import synth  # noqa: E402
 from parity import assert_parity, compare, sample_rows, u16  # noqa: E402
+from gpu_util import host, make_ctx, oracle_rows  # noqa: E402,F401
 
 pytestmark = pytest.mark.gpu
 
@@ -40,36 +41,6 @@ def dev():
 @pytest.fixture(scope="session")
 def O():
     return oracle.Oracle()
-
-
-def make_ctx(**env):
-    """A context created under the given FARN_* environment (read at create)."""
-    old = {k: os.environ.get(k) for k in env}
-    try:
-        for k, v in env.items():
-            os.environ[k] = str(v)
-        return farn.Context(0)
-    finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
-
-
-def host(t):
-    """Partials for the oracle: bf16 patterns, or fp32 values as they are."""
-    if t.dtype == torch.float32:
-        return t.detach().cpu().numpy()
-    return u16(t)
-
-
-def oracle_rows(O, xs, res, w, eps, rows=None):
-    if rows is None:
-        return O.forward([host(x) for x in xs], u16(res), u16(w), eps)
-    idx = torch.as_tensor(rows, device=res.device)
-    return O.forward([host(x.index_select(0, idx)) for x in xs],
-                     u16(res.index_select(0, idx)), u16(w), eps)
 
 
 def run_and_check(O, p, dev, ctx=None, rows=None, what=""):

@@ -20,7 +20,7 @@ import oracle  # noqa: E402
 import rank_sum_residual_gb300 as farn  # noqa: E402
 import synth  # noqa: E402
 from parity import assert_parity, u16  # noqa: E402
-from test_gpu_parity import make_ctx, oracle_rows  # noqa: E402
+from gpu_util import make_ctx, oracle_rows  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
