@@ -793,6 +793,8 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   prm.err = ctx->d_status;
   prm.stages = pl.stages;
   prm.stage_stride = pl.stage_stride;
+  prm.prefetch = (pl.variant == kVariantRow || pl.variant == kVariantCluster) &&
+                 T < ctx->small_t && ctx->pdl;
 
   DeviceGuard dg(ctx->device);
   if (!dg.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
