@@ -333,12 +333,14 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
     int cs = 1;
     if (ctx->force_cluster > 0 && want != kVariantRow) {
       cs = ctx->force_cluster;
-    } else if (want != kVariantRow && small && T < kClusterRowsMax) {
-      // A handful of rows: split each row over a cluster so that every
-      // CTA owns about 64 16-byte vectors, spreading the row's loads over
-      // up to 8 SMs.  (Measured on GB300: best below 8 rows; from 8 rows
-      // one CTA per row with every thread loading all ranks at once is as
-      // fast and needs no cluster barrier.)
+    } else if (want != kVariantRow && small && T < kClusterRowsMax && hv > 512) {
+      // A handful of long rows: split each row over a cluster so that every
+      // CTA owns about 64 16-byte vectors and each thread one vector of
+      // every rank, spreading the row's loads over up to 8 SMs.  Rows of
+      // up to 512 vectors (H <= 4096) stay in one CTA of one vector per
+      // thread: with the L2 prefetch before the wait that measured faster
+      // on GB300 (T = 1, 2, 4 at H = 4096: 2.63 us against 2.70-2.73 us for
+      // the 8-CTA split; from 8 rows one CTA per row was already as fast).
       const int cap = ctx->max_cluster < 8 ? ctx->max_cluster : 8;
       // (The NVFP4 output pairs vectors 2m, 2m+1 inside a CTA: even slices.)
       while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64 &&

@@ -224,8 +224,9 @@ def test_plan_choices(dev):
         assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
         assert plan(8, 1023, 8192)[0] == "row"
         assert plan(4, 1024, 5120)[0] == "row"          # 52 MB
-        assert plan(8, 1, 4096)[0] == "cluster"
-        assert plan(8, 1, 4096)[1] == 8
+        assert plan(8, 1, 4096) == ("row", 1, 512)     # one CTA of 512 threads
+        assert plan(8, 1, 8192)[0] == "cluster"         # longer rows: split
+        assert plan(8, 1, 8192)[1] == 8
         assert plan(8, 64, 4096) == ("row", 1, 512)     # decode: all ranks at once
         assert plan(4, 16, 13)[0] == "generic"          # H % 8 != 0
         assert plan(4, 16, 2048, off=2)[0] == "generic"  # misaligned
@@ -587,7 +588,8 @@ def test_f32_partials_plan(dev):
         args = ([a] * 8, a + g, a + 2 * g, a + 3 * g, a + 4 * g, a + 5 * g)
         assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 8192, 8192, *args)[0] == "row"
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 8192, *args)[0] == "stage"
-        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 2, 4096, *args)[0] == "cluster"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 2, 4096, *args)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 2, 8192, *args)[0] == "cluster"
         with pytest.raises(farn.FarnError):
             farn.farn_plan_typed(c.handle, 7, 8, 2, 4096, *args)
         # with the FP8 output (norm_out written or not) the same kernel choice
