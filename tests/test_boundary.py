@@ -150,3 +150,30 @@ def test_synth_twin_recipe_statistics():
     # different streams differ, same stream repeats
     assert not np.array_equal(xs[0], xs[1])
     assert np.array_equal(synth.host_bf16(1000, 0, 3, p.x), synth.host_bf16(1000, 0, 3, p.x))
+
+
+def test_synth_splitmix64_published_vectors():
+    """The generator's mixing function is SplitMix64's: with the state
+    advanced by the golden gamma from 0 it gives the published first outputs
+    0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F."""
+    import numpy as np
+    import synth
+    with np.errstate(over="ignore"):
+        got = [int(synth._mix64(np.uint64(k) * synth.GAMMA)) for k in (1, 2, 3)]
+    assert got == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_synth_moe_routing():
+    """Every expert-output row is gathered exactly once, gates are a softmax
+    (positive, summing to 1 per token), and the routing is seeded."""
+    import numpy as np
+    import synth
+    p = synth.workload("moe_combine")[0].with_T(300)
+    index, gates = synth.moe_routing(p)
+    assert index.shape == (300, p.W) and index.dtype == np.int32
+    assert np.array_equal(np.sort(index.ravel()), np.arange(300 * p.W))
+    assert (gates > 0).all() and np.allclose(gates.sum(axis=1), 1.0, atol=1e-6)
+    i2, g2 = synth.moe_routing(p)
+    assert np.array_equal(index, i2) and np.array_equal(gates, g2)
+    i3, _ = synth.moe_routing(p.with_seed(p.seed + 1))
+    assert not np.array_equal(index, i3)

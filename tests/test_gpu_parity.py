@@ -954,3 +954,22 @@ def test_moe_combine_in_place_and_aliasing(O, dev):
     with pytest.raises(farn.FarnError) as e:       # output over an expert row
         farn.moe_combine(ex, index, gates, res, w, p.eps, out=(ex[:20], red, nrm))
     assert e.value.status == farn.FARN_ERR_ALIAS
+
+
+@pytest.mark.parametrize("name", ["prefill", "wide", "prefill_f32"])
+def test_synth_device_fill_matches_host_twin(dev, name):
+    """The device generator and its numpy twin follow one recipe: the same
+    bytes, up to a rare last-bit difference of the fp64 transcendental
+    functions surviving the rounding to fp32 (and bf16)."""
+    p = synth.workload(name)[0].with_T(128)
+    xs_d, res_d, w_d = synth.device_inputs(p, dev)
+    xs_h, res_h, w_h = synth.host_inputs(p)
+    pairs = [(host(x), xh) for x, xh in zip(xs_d, xs_h)] + [(u16(res_d), res_h), (u16(w_d), w_h)]
+    n = bad = 0
+    for a, b in pairs:
+        a, b = np.asarray(a).ravel(), np.asarray(b).ravel()
+        assert a.shape == b.shape
+        n += a.size
+        bad += int(np.count_nonzero(a.view(np.uint16 if a.dtype == np.uint16 else np.uint32)
+                                    != b.view(np.uint16 if b.dtype == np.uint16 else np.uint32)))
+    assert bad <= max(2, n // 100000), f"{bad} of {n} generated values differ"
