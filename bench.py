@@ -664,41 +664,22 @@ def call_forward(p, xs, res, w, outs, ctx, stream):
 
 
 def prepare_call(p, xs, res, w, outs, ctx, stream):
-    """One operator call through the C ABI with its arguments marshalled
-    once (the pointer array and the ctypes values), returned as a function
-    of no arguments that makes the call and returns its status: the
-    per-call host cost of a caller that keeps its buffers."""
-    import ctypes
+    """One call of the workload through the binding's prepared-call API:
+    tensors checked and C-ABI arguments marshalled once, then each call is
+    only the C call (the per-call host cost of a caller that keeps its
+    buffers)."""
     import rank_sum_residual_gb300 as farn
-    lib = farn._load()
-    vp = ctypes.c_void_p
-    h = vp((ctx or farn._context_for(res.device.index)).handle)
-    st = vp(int(stream.cuda_stream))
-    ptr = lambda t: vp(t.data_ptr()) if t is not None else None  # noqa: E731
     if p.kind == "moe_combine":
         ex, index, gates = xs
-        args = (h, ptr(ex), ctypes.c_int64(ex.shape[0]), ptr(index), ptr(gates),
-                ctypes.c_int(p.W), ptr(res), ptr(w), ctypes.c_float(p.eps),
-                ctypes.c_int64(p.T), ctypes.c_int64(p.H), ptr(outs[0]), ptr(outs[1]),
-                ptr(outs[2]), st)
-        fn = lib.farn_moe_combine
-    else:
-        arr = farn._ptr_array([x.data_ptr() for x in xs])
-        dt = ctypes.c_int(farn.FARN_F32 if p.partial_bytes == 4 else farn.FARN_BF16)
-        common = (h, arr, dt, ctypes.c_int(p.W), ptr(res), ptr(w), ctypes.c_float(p.eps),
-                  ctypes.c_int64(p.T), ctypes.c_int64(p.H))
-        if p.nvfp4_out:
-            args = common + (ctypes.c_float(p.tensor_scale), ptr(outs[0]), ptr(outs[1]),
-                             ptr(outs[2]), ptr(outs[3]), ptr(outs[4]), st)
-            fn = lib.farn_forward_nvfp4
-        elif p.fp8_out:
-            args = common + (ptr(outs[0]), ptr(outs[1]), ptr(outs[2]), ptr(outs[3]),
-                             ptr(outs[4]), st)
-            fn = lib.farn_forward_quant
-        else:
-            args = common + (ptr(outs[0]), ptr(outs[1]), ptr(outs[2]), st)
-            fn = lib.farn_forward_typed
-    return lambda: fn(*args)                      # args holds the pointer array
+        return farn.prepare_moe_combine(ex, index, gates, res, w, p.eps, out=tuple(outs[:3]),
+                                        ctx=ctx, stream=stream)
+    if p.nvfp4_out:
+        return farn.prepare_forward_nvfp4(xs, res, w, p.eps, p.tensor_scale, p.norm_out,
+                                          out=tuple(outs), ctx=ctx, stream=stream)
+    if p.fp8_out:
+        return farn.prepare_forward_quant(xs, res, w, p.eps, p.norm_out, out=tuple(outs),
+                                          ctx=ctx, stream=stream)
+    return farn.prepare_forward(xs, res, w, p.eps, out=tuple(outs[:3]), ctx=ctx, stream=stream)
 
 
 def time_calls_alone(problems, dev, ctx, l2_bytes, min_launches=64):
@@ -826,10 +807,8 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
         ev["in"][j].record(s_in)
         s_comp.wait_event(ev["in"][j])
         s_comp.wait_event(ev["out"][j])            # slot's outputs copied out
-        for fn in prepared[j]:
-            st = fn()
-            if st != 0:
-                raise farn.FarnError(st, "farn call in the end-to-end step")
+        for call in prepared[j]:
+            call()
         ev["comp"][j].record(s_comp)
         s_out.wait_event(ev["comp"][j])
         with torch.cuda.stream(s_out):
@@ -863,7 +842,8 @@ def run_e2e(calls, problems, stream, dev, K, world, step_bytes):
             "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
             "steps": Ke, "ms_per_step": ms / Ke,
             "path": "per step: one pinned-host -> device copy of all inputs, "
-                    "every call through the C ABI (ctypes, arguments marshalled once), one "
+                    "every call through the binding's prepared calls (C ABI, arguments "
+                    "checked and marshalled once), one "
                     "device -> pinned-host copy of all three outputs; copy-in, compute "
                     "and copy-out on three streams over two buffer slots"}
 

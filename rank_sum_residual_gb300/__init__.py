@@ -190,36 +190,6 @@ def farn_moe_combine(ctx, expert_out, n_slots, index, gates, K, residual, weight
         v(residual_out), v(norm_out), ctypes.c_void_p(int(stream)))
 
 
-def moe_combine(expert_out, index, gates, residual, weight, eps: float, out=None, ctx=None,
-                stream=None):
-    """MoE combine + residual + RMSNorm on torch CUDA tensors: expert_out bf16
-    [S,H], index int32 [T,K], gates fp32 [T,K], residual bf16 [T,H], weight
-    bf16 [H].  Returns (reduced, residual_out, norm_out)."""
-    import torch
-    T, H = residual.shape
-    dev = residual.device
-    S = expert_out.shape[0]
-    _check_tensor(expert_out, "expert_out", (S, H), dev)
-    K = index.shape[1] if index.dim() == 2 else -1
-    _check_tensor(index, "index", (T, K), dev, (torch.int32,))
-    _check_tensor(gates, "gates", (T, K), dev, (torch.float32,))
-    _check_tensor(residual, "residual", (T, H), dev)
-    _check_tensor(weight, "weight", (H,), dev)
-    if out is None:
-        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(3))
-    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
-        _check_tensor(t, name, (T, H), dev)
-    c = ctx if ctx is not None else _context_for(dev.index)
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = farn_moe_combine(c.handle, expert_out.data_ptr(), S, index.data_ptr(), gates.data_ptr(),
-                          K, residual.data_ptr(), weight.data_ptr(), eps, T, H,
-                          out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
-                          s.cuda_stream)
-    if st != FARN_OK:
-        raise FarnError(st, "farn_moe_combine")
-    return out
-
-
 def farn_forward_noalloc(device, partials, W, residual, weight, eps, T, H,
                          reduced_out, residual_out, norm_out, stream=0,
                          want_status=False):
@@ -354,17 +324,33 @@ def _check_tensor(t, name, shape, device, dtypes=None):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def forward(partials, residual, weight, eps: float, out=None, ctx=None,
-            stream=None):
-    """The fused operator on torch CUDA tensors.
+# ------------------------------------------------------------ torch level
+class PreparedCall:
+    """One operator call whose tensors were checked and whose C-ABI
+    arguments were marshalled once.  Calling it launches the kernel on the
+    stream given at preparation (asynchronously) and returns the outputs; a
+    caller that reuses its buffers (a serving loop, a benchmark) pays only
+    the C call each time.  The tensors must stay alive, in place, while the
+    object is used."""
 
-    partials: sequence of W tensors [T,H], all bf16 or all fp32 (fp32 partials
-    are summed as fp32, see farn_forward_typed); residual [T,H] and weight
-    [H] bf16; outputs bf16.
-    out: optional (reduced, residual_out, norm_out) tensors to write
-    (residual_out may be ``residual`` itself).  Runs asynchronously on
-    ``stream`` (default: torch's current stream) and returns the outputs.
-    """
+    __slots__ = ("_fn", "_args", "_name", "_keep", "outputs")
+
+    def __init__(self, fn, args, name, outputs, keep):
+        self._fn, self._args, self._name = fn, args, name
+        self.outputs, self._keep = outputs, keep
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != FARN_OK:
+            raise FarnError(st, self._name)
+        return self.outputs
+
+
+def _vp(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _partials_checked(partials, residual, weight):
     import torch
     partials = list(partials)
     if not partials:
@@ -380,21 +366,81 @@ def forward(partials, residual, weight, eps: float, out=None, ctx=None,
         _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
     _check_tensor(residual, "residual", (T, H), dev)
     _check_tensor(weight, "weight", (H,), dev)
-    if out is None:
-        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-                    for _ in range(3))
-    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
-        _check_tensor(t, name, (T, H), dev)
+    return partials, T, H, dev, (FARN_F32 if pdt == torch.float32 else FARN_BF16)
+
+
+def _common_args(ctx, partials, dtype, residual, weight, eps, T, H):
+    return (ctypes.c_void_p(ctx.handle), _ptr_array([x.data_ptr() for x in partials]),
+            ctypes.c_int(dtype), ctypes.c_int(len(partials)), _vp(residual), _vp(weight),
+            ctypes.c_float(eps), ctypes.c_int64(T), ctypes.c_int64(H))
+
+
+def _ctx_stream(ctx, stream, dev):
+    import torch
     c = ctx if ctx is not None else _context_for(dev.index)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = farn_forward_typed(c.handle, [x.data_ptr() for x in partials],
-                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
-                            residual.data_ptr(), weight.data_ptr(), eps, T, H,
-                            out[0].data_ptr(), out[1].data_ptr(), out[2].data_ptr(),
-                            s.cuda_stream)
-    if st != FARN_OK:
-        raise FarnError(st, "farn_forward")
-    return out
+    return c, ctypes.c_void_p(int(s.cuda_stream))
+
+
+def prepare_forward(partials, residual, weight, eps: float, out=None, ctx=None, stream=None):
+    """``forward`` checked and marshalled once (see ``PreparedCall``)."""
+    import torch
+    partials, T, H, dev, dtype = _partials_checked(partials, residual, weight)
+    if out is None:
+        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
+        _check_tensor(t, name, (T, H), dev)
+    c, s = _ctx_stream(ctx, stream, dev)
+    args = _common_args(c, partials, dtype, residual, weight, eps, T, H) + \
+        (_vp(out[0]), _vp(out[1]), _vp(out[2]), s)
+    return PreparedCall(_load().farn_forward_typed, args, "farn_forward", tuple(out),
+                        (partials, residual, weight, c))
+
+
+def forward(partials, residual, weight, eps: float, out=None, ctx=None,
+            stream=None):
+    """The fused operator on torch CUDA tensors.
+
+    partials: sequence of W tensors [T,H], all bf16 or all fp32 (fp32 partials
+    are summed as fp32, see farn_forward_typed); residual [T,H] and weight
+    [H] bf16; outputs bf16.
+    out: optional (reduced, residual_out, norm_out) tensors to write
+    (residual_out may be ``residual`` itself).  Runs asynchronously on
+    ``stream`` (default: torch's current stream) and returns the outputs.
+    """
+    return prepare_forward(partials, residual, weight, eps, out, ctx, stream)()
+
+
+def _check_quant_out(out, T, H, dev, q_shape, q_dtype, s_shape, s_dtype):
+    import torch
+    if len(out) != 5:
+        raise ValueError("out must be (reduced, residual_out, norm_out or None, codes, scales)")
+    for name, t in zip(("reduced", "residual_out"), out[:2]):
+        _check_tensor(t, name, (T, H), dev)
+    if out[2] is not None:
+        _check_tensor(out[2], "norm_out", (T, H), dev)
+    _check_tensor(out[3], "codes", q_shape, dev, (q_dtype,))
+    _check_tensor(out[4], "scales", s_shape, dev, (s_dtype,))
+
+
+def prepare_forward_quant(partials, residual, weight, eps: float, write_norm: bool = True,
+                          out=None, ctx=None, stream=None):
+    """``forward_quant`` checked and marshalled once.  out: optional
+    (reduced, residual_out, norm_out or None, norm_q, row_scale)."""
+    import torch
+    partials, T, H, dev, dtype = _partials_checked(partials, residual, weight)
+    if out is None:
+        out = (torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None,
+               torch.empty((T, H), dtype=torch.uint8, device=dev),
+               torch.empty((T,), dtype=torch.float32, device=dev))
+    _check_quant_out(out, T, H, dev, (T, H), torch.uint8, (T,), torch.float32)
+    c, s = _ctx_stream(ctx, stream, dev)
+    args = _common_args(c, partials, dtype, residual, weight, eps, T, H) + \
+        tuple(_vp(t) for t in out) + (s,)
+    return PreparedCall(_load().farn_forward_quant, args, "farn_forward_quant", tuple(out),
+                        (partials, residual, weight, c))
 
 
 def forward_quant(partials, residual, weight, eps: float, write_norm: bool = True,
@@ -402,34 +448,30 @@ def forward_quant(partials, residual, weight, eps: float, write_norm: bool = Tru
     """``forward`` plus the FP8 (E4M3) copy of norm_out and its per-row
     scales.  Returns (reduced, residual_out, norm_out or None, norm_q as a
     uint8 tensor of E4M3 patterns, row_scale float32 [T])."""
+    return prepare_forward_quant(partials, residual, weight, eps, write_norm,
+                                 ctx=ctx, stream=stream)()
+
+
+def prepare_forward_nvfp4(partials, residual, weight, eps: float, tensor_scale: float,
+                          write_norm: bool = True, out=None, ctx=None, stream=None):
+    """``forward_nvfp4`` checked and marshalled once.  out: optional
+    (reduced, residual_out, norm_out or None, norm_fp4, block_scale)."""
     import torch
-    partials = list(partials)
-    if not partials:
-        raise ValueError("partials must hold at least one tensor")
-    T, H = residual.shape
-    dev = residual.device
-    pdt = partials[0].dtype
-    if pdt not in (torch.bfloat16, torch.float32):
-        raise TypeError(f"partials must be bfloat16 or float32, got {pdt}")
-    for r, x in enumerate(partials):
-        _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
-    _check_tensor(residual, "residual", (T, H), dev)
-    _check_tensor(weight, "weight", (H,), dev)
-    red = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    nrm = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None
-    q = torch.empty((T, H), dtype=torch.uint8, device=dev)
-    scale = torch.empty((T,), dtype=torch.float32, device=dev)
-    c = ctx if ctx is not None else _context_for(dev.index)
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = farn_forward_quant(c.handle, [x.data_ptr() for x in partials],
-                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
-                            residual.data_ptr(), weight.data_ptr(), eps, T, H,
-                            red.data_ptr(), ro.data_ptr(), nrm.data_ptr() if nrm is not None else 0,
-                            q.data_ptr(), scale.data_ptr(), s.cuda_stream)
-    if st != FARN_OK:
-        raise FarnError(st, "farn_forward_quant")
-    return red, ro, nrm, q, scale
+    partials, T, H, dev, dtype = _partials_checked(partials, residual, weight)
+    if H % 16:
+        raise ValueError(f"NVFP4 output needs H % 16 == 0, got H = {H}")
+    if out is None:
+        out = (torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, H), dtype=torch.bfloat16, device=dev),
+               torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None,
+               torch.empty((T, H // 2), dtype=torch.uint8, device=dev),
+               torch.empty((T, H // 16), dtype=torch.uint8, device=dev))
+    _check_quant_out(out, T, H, dev, (T, H // 2), torch.uint8, (T, H // 16), torch.uint8)
+    c, s = _ctx_stream(ctx, stream, dev)
+    args = _common_args(c, partials, dtype, residual, weight, eps, T, H) + \
+        (ctypes.c_float(tensor_scale),) + tuple(_vp(t) for t in out) + (s,)
+    return PreparedCall(_load().farn_forward_nvfp4, args, "farn_forward_nvfp4", tuple(out),
+                        (partials, residual, weight, c))
 
 
 def forward_nvfp4(partials, residual, weight, eps: float, tensor_scale: float,
@@ -438,33 +480,39 @@ def forward_nvfp4(partials, residual, weight, eps: float, tensor_scale: float,
     residual_out, norm_out or None, norm_fp4 uint8 [T,H/2] (two E2M1 codes
     per byte, the even element in the low nibble), block_scale uint8
     [T,H/16] (E4M3 patterns)).  H must be a multiple of 16."""
+    return prepare_forward_nvfp4(partials, residual, weight, eps, tensor_scale, write_norm,
+                                 ctx=ctx, stream=stream)()
+
+
+def prepare_moe_combine(expert_out, index, gates, residual, weight, eps: float, out=None,
+                        ctx=None, stream=None):
+    """``moe_combine`` checked and marshalled once."""
     import torch
-    partials = list(partials)
-    if not partials:
-        raise ValueError("partials must hold at least one tensor")
     T, H = residual.shape
-    if H % 16:
-        raise ValueError(f"NVFP4 output needs H % 16 == 0, got H = {H}")
     dev = residual.device
-    pdt = partials[0].dtype
-    if pdt not in (torch.bfloat16, torch.float32):
-        raise TypeError(f"partials must be bfloat16 or float32, got {pdt}")
-    for r, x in enumerate(partials):
-        _check_tensor(x, f"partials[{r}]", (T, H), dev, (pdt,))
+    S = expert_out.shape[0]
+    _check_tensor(expert_out, "expert_out", (S, H), dev)
+    K = index.shape[1] if index.dim() == 2 else -1
+    _check_tensor(index, "index", (T, K), dev, (torch.int32,))
+    _check_tensor(gates, "gates", (T, K), dev, (torch.float32,))
     _check_tensor(residual, "residual", (T, H), dev)
     _check_tensor(weight, "weight", (H,), dev)
-    red = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    ro = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    nrm = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if write_norm else None
-    q = torch.empty((T, H // 2), dtype=torch.uint8, device=dev)
-    sc = torch.empty((T, H // 16), dtype=torch.uint8, device=dev)
-    c = ctx if ctx is not None else _context_for(dev.index)
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    st = farn_forward_nvfp4(c.handle, [x.data_ptr() for x in partials],
-                            FARN_F32 if pdt == torch.float32 else FARN_BF16, len(partials),
-                            residual.data_ptr(), weight.data_ptr(), eps, T, H, tensor_scale,
-                            red.data_ptr(), ro.data_ptr(), nrm.data_ptr() if nrm is not None else 0,
-                            q.data_ptr(), sc.data_ptr(), s.cuda_stream)
-    if st != FARN_OK:
-        raise FarnError(st, "farn_forward_nvfp4")
-    return red, ro, nrm, q, sc
+    if out is None:
+        out = tuple(torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(3))
+    for name, t in zip(("reduced", "residual_out", "norm_out"), out):
+        _check_tensor(t, name, (T, H), dev)
+    c, s = _ctx_stream(ctx, stream, dev)
+    args = (ctypes.c_void_p(c.handle), _vp(expert_out), ctypes.c_int64(S), _vp(index),
+            _vp(gates), ctypes.c_int(K), _vp(residual), _vp(weight), ctypes.c_float(eps),
+            ctypes.c_int64(T), ctypes.c_int64(H), _vp(out[0]), _vp(out[1]), _vp(out[2]), s)
+    return PreparedCall(_load().farn_moe_combine, args, "farn_moe_combine", tuple(out),
+                        (expert_out, index, gates, residual, weight, c))
+
+
+def moe_combine(expert_out, index, gates, residual, weight, eps: float, out=None, ctx=None,
+                stream=None):
+    """MoE combine + residual + RMSNorm on torch CUDA tensors: expert_out bf16
+    [S,H], index int32 [T,K], gates fp32 [T,K], residual bf16 [T,H], weight
+    bf16 [H].  Returns (reduced, residual_out, norm_out)."""
+    return prepare_moe_combine(expert_out, index, gates, residual, weight, eps, out, ctx,
+                               stream)()

@@ -973,3 +973,33 @@ def test_synth_device_fill_matches_host_twin(dev, name):
         bad += int(np.count_nonzero(a.view(np.uint16 if a.dtype == np.uint16 else np.uint32)
                                     != b.view(np.uint16 if b.dtype == np.uint16 else np.uint32)))
     assert bad <= max(2, n // 100000), f"{bad} of {n} generated values differ"
+
+
+def test_prepared_calls_reuse_their_buffers(O, dev):
+    """A prepared call, launched again after its inputs change in place,
+    gives the oracle's results each time; the prepared FP8, NVFP4 and MoE
+    calls give the same bytes as the immediate functions."""
+    p = synth.workload("prefill")[0].with_T(300)
+    xs, res, w = synth.device_inputs(p, dev)
+    call = farn.prepare_forward(xs, res, w, p.eps)
+    for k in range(2):
+        if k:
+            synth.fill_device(xs[1], 77, 1, p.x)
+        out = call()
+        torch.cuda.synchronize()
+        assert_parity([u16(t) for t in out], oracle_rows(O, xs, res, w, p.eps), f"prepared {k}")
+    q8 = farn.prepare_forward_quant(xs, res, w, p.eps)()
+    q4 = farn.prepare_forward_nvfp4(xs, res, w, p.eps, 168.0, write_norm=False)()
+    a8 = farn.forward_quant(xs, res, w, p.eps)
+    a4 = farn.forward_nvfp4(xs, res, w, p.eps, 168.0, write_norm=False)
+    pm = _moe(200, 8, 2048, seed=5)
+    (ex, index, gates), mres, mw = synth.device_inputs(pm, dev)
+    m1 = farn.prepare_moe_combine(ex, index, gates, mres, mw, pm.eps)()
+    m2 = farn.moe_combine(ex, index, gates, mres, mw, pm.eps)
+    torch.cuda.synchronize()
+    for got, want in ((q8, a8), (q4, a4), (m1, m2)):
+        for a, b in zip(got, want):
+            assert (a is None and b is None) or torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    with pytest.raises(ValueError):
+        bad = (q8[0], q8[1], q8[2], q8[3][:, :10], q8[4])   # codes of the wrong shape
+        farn.prepare_forward_quant(xs, res, w, p.eps, out=bad)
