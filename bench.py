@@ -5,9 +5,12 @@
                     [--impl farn|reference]
 
 One step is one pass of the whole operator over one batch of the workload:
-for the default workload, the decode sweep (W=8, H=4096), one call for each
-T in 1,2,4,...,128 (255 rows); for the others, one call on the full
-[T,H] problem.  Inputs are seeded synthetic bf16 tensors generated on the
+for the default workload, the largest benchmark configuration (W=4,
+T=32768, H=5120: 2.68 GB per call), one call on the full [T,H] problem; for
+the decode sweep (W=8, H=4096), one call for each T in 1,2,4,...,128 (255
+rows).  The headline workload runs exactly --steps timed steps; then every
+other benchmark configuration (c1, decode, prefill, nonpow2, wide) is timed
+in the same run and reported under "configs" (--only skips them).  Inputs are seeded synthetic bf16 tensors generated on the
 device (synth/), rotated over enough copies that one pass over all copies
 is more than twice the L2 cache, so every call reads HBM.
 
@@ -47,7 +50,10 @@ if ROOT not in sys.path:
 METRIC = "effective HBM GB/s and rows/s (1×GB300) as % of HBM peak, vs CPU oracle"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_WORKLOAD = "decode"
+DEFAULT_WORKLOAD = "nonpow2"
+# The benchmark configurations: a small call, the decode sweep, prefill, a
+# non-power-of-two hidden size and a wide reduction.
+BENCH_CONFIGS = ("c1", "decode", "prefill", "nonpow2", "wide")
 
 
 def parse_args(argv=None):
@@ -71,6 +77,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--rows", type=int, default=None,
                     help="override T of every call (small cases for profiling)")
+    ap.add_argument("--only", action="store_true",
+                    help="time the --workload alone, not the other benchmark configurations")
+    ap.add_argument("--config-ms", type=float, default=300.0,
+                    help="timed GPU work per extra configuration, ms")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0,
+                    help="CPU oracle work per extra configuration")
     return ap.parse_args(argv)
 
 
@@ -339,8 +351,171 @@ def workload_desc(name, problems):
 
 
 # ------------------------------------------------------------------ GPU
+def setup_sets(problems, dev, stream, l2, in_place):
+    """Rotating device copies of one workload's inputs and outputs, enough
+    that one pass over all of them is more than twice the L2 size."""
+    import torch
+    import synth
+    set_bytes = sum(p.algorithmic_bytes() for p in problems)
+    n_sets = max(2, math.ceil(2 * l2 / set_bytes))
+    n_sets = min(n_sets, max(1, int(40e9 // set_bytes)))
+    sets = []
+    with torch.cuda.stream(stream):
+        for k in range(n_sets):
+            calls = []
+            for p in problems:
+                xs, res, w = synth.device_inputs(p, dev, seed=p.seed + 7919 * k)
+                outs = make_outputs(p, dev)
+                if in_place:
+                    # residual_out is the residual buffer itself; every step
+                    # then reads the residual the previous step over that
+                    # copy wrote, which leaves the bytes moved unchanged
+                    outs = (outs[0], res) + tuple(outs[2:])
+                calls.append((p, xs, res, w, outs))
+            sets.append(calls)
+    stream.synchronize()
+    return sets, set_bytes
+
+
+class StepRunner:
+    """Steps of one workload over its rotating input copies.  One CUDA graph
+    replay is one rotation (n_sets steps), plus a one-step graph per copy,
+    so exactly the requested number of steps is run and the host never
+    paces the GPU."""
+
+    def __init__(self, sets, ctx, stream, use_graph):
+        import torch
+        self.sets, self.ctx, self.stream = sets, ctx, stream
+        self.n_sets = len(sets)
+        self.use_graph = use_graph
+        self.graph, self.step_graphs, self.pos = None, [], 0
+        if use_graph:
+            self.graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.graph, stream=stream):
+                for k in range(self.n_sets):
+                    self.step(k)
+            for k in range(self.n_sets):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    self.step(k)
+                self.step_graphs.append(g)
+            self.graph.replay()
+            for g in self.step_graphs:
+                g.replay()
+            stream.synchronize()
+
+    def step(self, k):
+        for p, xs, res, w, outs in self.sets[k]:
+            call_forward(p, xs, res, w, outs, self.ctx, self.stream)
+
+    def run(self, n):
+        """Exactly n steps, continuing the rotation over the input copies."""
+        while n > 0:
+            if self.use_graph and self.pos == 0 and n >= self.n_sets:
+                self.graph.replay()
+                n -= self.n_sets
+                continue
+            if self.use_graph:
+                self.step_graphs[self.pos].replay()
+            else:
+                self.step(self.pos)
+            self.pos = (self.pos + 1) % self.n_sets
+            n -= 1
+
+
+def time_steps(runner, stream, dev, K, warmup, world, target_ms=1500.0):
+    """Warm-up, then exactly K steps (K None: about target_ms of GPU time)
+    timed with CUDA events on the launching stream, bracketed by a barrier
+    and a device synchronisation; the time is the maximum over ranks."""
+    import torch
+    n_sets = runner.n_sets
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    runner.run(max(warmup, 1))
+    stream.synchronize()
+    e0.record(stream)
+    runner.run(4 * n_sets)
+    e1.record(stream)
+    e1.synchronize()
+    calib_ms = e0.elapsed_time(e1) / (4 * n_sets)
+    if K is None:
+        K = max(20, int(target_ms / max(calib_ms, 1e-4)))
+        K = (K + n_sets - 1) // n_sets * n_sets
+    runner.run(warmup)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    # The K steps run back to back; events between consecutive chunks of
+    # them (recorded on the same stream, no gap added) give the spread.
+    n_chunks = max(1, min(20, K))
+    bounds = [round(K * i / n_chunks) for i in range(n_chunks + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
+    t_wall0 = time.time()
+    evs[0].record(stream)
+    for i in range(n_chunks):
+        runner.run(bounds[i + 1] - bounds[i])
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dev)
+    chunk_ms = sorted(evs[i].elapsed_time(evs[i + 1]) / (bounds[i + 1] - bounds[i])
+                      for i in range(n_chunks) if bounds[i + 1] > bounds[i])
+
+    def pct(q):
+        return chunk_ms[min(len(chunk_ms) - 1, int(q * (len(chunk_ms) - 1) + 0.5))]
+    stats = {"chunks": len(chunk_ms), "p10_ms": pct(0.1), "median_ms": pct(0.5),
+             "p90_ms": pct(0.9), "mean_ms": ms / K}
+    return K, ms, stats, calib_ms, (t_wall0, t_wall1)
+
+
+def annotate_calls(per_call, problems, sets, ctx, peak):
+    """Per-call GB/s, fraction of the peak and the kernel plan."""
+    import rank_sum_residual_gb300 as farn
+    for j, c in enumerate(per_call):
+        c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
+        c["frac"] = c["gbs"] / peak
+        c["rows_per_s"] = c["T"] / (c["kernel_us"] * 1e-6)
+        if problems[j].kind == "moe_combine":
+            _, (ex, _, _), res_j, w_j, outs_j = sets[0][j]
+            v, thr = farn.farn_plan_moe_combine(
+                ctx.handle, problems[j].W, problems[j].T, problems[j].H, ex.data_ptr(),
+                res_j.data_ptr(), w_j.data_ptr(), outs_j[0].data_ptr(), outs_j[1].data_ptr(),
+                outs_j[2].data_ptr())
+            c["variant"] = ("combine-stage" if v == "stage" else v) + f" threads={thr}"
+            continue
+        v, cs, thr = farn.farn_plan_typed(ctx.handle, *plan_args(sets[0][j]))
+        c["variant"] = f"{v} cluster={cs} threads={thr}"
+        c["kernel"] = kernel_name(c["variant"])
+
+
+# The acceptance bars on the fraction of the HBM roofline: long calls
+# (T >= 4096) at least 75 %, decode-sized calls (T <= 128) at least 40 %.
+def bar_for(T):
+    return 0.75 if T >= 4096 else (0.40 if T <= 128 else None)
+
+
+def config_summary(name, problems, K, ms, stats, calib_ms, per_call, n_sets, set_bytes, l2,
+                   peak, world, clocks):
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    step_rows = sum(p.T for p in problems)
+    secs = ms / 1e3
+    gbs = world * step_bytes * K / secs / 1e9
+    out = {"workload": workload_desc(name, problems), "steps": K, "ms_per_step": ms / K,
+           "bytes_per_step": step_bytes, "rows_per_step": step_rows,
+           "gbs": gbs, "frac": gbs / world / peak, "rows_per_s": world * step_rows * K / secs,
+           "step_ms_spread": stats, "calibration_ms_per_step": calib_ms,
+           "l2": f"inputs rotated over {n_sets} device copies "
+                 f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB); no flush",
+           "clocks": clocks,
+           "per_call": per_call}
+    bars = [(c["call"], bar_for(c["T"]), c["frac"]) for c in per_call if bar_for(c["T"])]
+    if bars:
+        out["bar"] = {c: {"target_frac": b, "frac": f, "met": f >= b} for c, b, f in bars}
+    return out
+
+
 def run_gpu(args):
-    import numpy as np
     import torch
 
     import rank_sum_residual_gb300 as farn
@@ -357,174 +532,89 @@ def run_gpu(args):
     synth.build()
 
     peak, peak_src = hbm_peak()
-    problems = synth.workload(args.workload)
-    if args.rows is not None:
-        problems = [p.with_T(args.rows) for p in problems]
-    step_bytes = sum(p.algorithmic_bytes() for p in problems)
-    step_rows = sum(p.T for p in problems)
-    set_bytes = step_bytes  # algorithmic bytes touched by one pass over one set
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_sets = max(2, math.ceil(2 * l2 / set_bytes))
-    n_sets = min(n_sets, max(1, int(40e9 // set_bytes)))
     ctx = farn.Context(local)
     # One stream for everything: torch's graph replay, the calls and every
     # CUDA event all use torch's current stream, so make it this one.
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
-
-    # ---- inputs: n_sets rotating copies, generated on the device
-    sets = []
-    with torch.cuda.stream(stream):
-        for k in range(n_sets):
-            calls = []
-            for p in problems:
-                xs, res, w = synth.device_inputs(p, dev, seed=p.seed + 7919 * k)
-                outs = make_outputs(p, dev)
-                if args.in_place:
-                    # residual_out is the residual buffer itself; every step
-                    # then reads the residual the previous step over that
-                    # copy wrote, which leaves the bytes moved unchanged
-                    outs = (outs[0], res) + tuple(outs[2:])
-                calls.append((p, xs, res, w, outs))
-            sets.append(calls)
-    stream.synchronize()
-
-    def launch(call):
-        p, xs, res, w, outs = call
-        call_forward(p, xs, res, w, outs, ctx, stream)
-
-    def step(k):
-        for call in sets[k]:
-            launch(call)
-
-    # ---- warm-up (also loads every kernel before capture)
-    for i in range(max(args.warmup, 1)):
-        step(i % n_sets)
-    stream.synchronize()
-
-    # ---- CUDA graph: one replay is one rotation, i.e. one step over every
-    # input copy in turn (n_sets steps), so the host issues one replay per
-    # n_sets steps and never paces the GPU.
-    # Plus one graph per copy (one step each) for step counts that are not
-    # whole rotations: exactly the requested number of steps is run.
     use_graph = not args.no_graph
-    graph, step_graphs = None, []
-    if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for k in range(n_sets):
-                step(k)
-        for k in range(n_sets):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                step(k)
-            step_graphs.append(g)
-        graph.replay()
-        for g in step_graphs:
-            g.replay()
-        stream.synchronize()
-    pos = [0]          # input copy the next step uses
 
-    def run_steps(n):
-        """Exactly n steps, continuing the rotation over the input copies."""
-        while n > 0:
-            if use_graph and pos[0] == 0 and n >= n_sets:
-                graph.replay()
-                n -= n_sets
-                continue
-            if use_graph:
-                step_graphs[pos[0]].replay()
-            else:
-                step(pos[0])
-            pos[0] = (pos[0] + 1) % n_sets
-            n -= 1
-
-    # ---- step count: about 1.5 s of GPU time unless given
-    K = args.steps
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    run_steps(4 * n_sets)
-    e1.record(stream)
-    e1.synchronize()
-    calib_ms = e0.elapsed_time(e1) / (4 * n_sets)
-    if K is None:
-        K = max(20, int(1500.0 / max(calib_ms, 1e-4)))
-        K = (K + n_sets - 1) // n_sets * n_sets
+    def load(name):
+        problems = synth.workload(name)
+        if args.rows is not None:
+            problems = [p.with_T(args.rows) for p in problems]
+        return problems
 
     sampler = ClockSampler(gpu_id_for(local)).start() if rank == 0 else None
     time.sleep(0.5 if sampler else 0)
-    run_steps(args.warmup)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    # The K steps run back to back; events between consecutive chunks of
-    # them (recorded on the same stream, no gap added) give the spread.
-    n_chunks = max(1, min(20, K // max(1, n_sets)))
-    bounds = [round(K * i / n_chunks) for i in range(n_chunks + 1)]
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
-    t_wall0 = time.time()
-    evs[0].record(stream)
-    for i in range(n_chunks):
-        run_steps(bounds[i + 1] - bounds[i])
-        evs[i + 1].record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = max_over_ranks(evs[0].elapsed_time(evs[-1]), dev)
-    chunk_ms = sorted(evs[i].elapsed_time(evs[i + 1]) / (bounds[i + 1] - bounds[i])
-                      for i in range(n_chunks) if bounds[i + 1] > bounds[i])
 
-    def pct(q):
-        return chunk_ms[min(len(chunk_ms) - 1, int(q * (len(chunk_ms) - 1) + 0.5))]
-    step_stats = {"chunks": len(chunk_ms), "p10_ms": pct(0.1), "median_ms": pct(0.5),
-                  "p90_ms": pct(0.9), "mean_ms": ms / K}
-
-    # ---- per-call kernel time, right after the timed steps and under the
-    # same clock sampling: each call alone, back to back over the input
-    # copies in one CUDA graph, CUDA events on the launching stream.
+    # ---- the headline workload: exactly --steps timed steps after --warmup
+    problems = load(args.workload)
+    step_bytes = sum(p.algorithmic_bytes() for p in problems)
+    step_rows = sum(p.T for p in problems)
+    sets, set_bytes = setup_sets(problems, dev, stream, l2, args.in_place)
+    runner = StepRunner(sets, ctx, stream, use_graph)
+    K, ms, step_stats, calib_ms, (t_wall0, t_wall1) = time_steps(
+        runner, stream, dev, args.steps, args.warmup, world)
+    # per-call kernel time, right after the timed steps and under the same
+    # clock sampling: each call alone, back to back over its own input copies
     per_call = time_calls_alone(problems, dev, ctx, l2)
-    time.sleep(0.3 if sampler else 0)
-    if sampler:
-        sampler.stop()
+    annotate_calls(per_call, problems, sets, ctx, peak)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
     secs = ms / 1e3
     value = world * step_bytes * K / secs / 1e9
     rows_per_s = world * step_rows * K / secs
-
-    for j, c in enumerate(per_call):
-        c["gbs"] = c["bytes"] / (c["kernel_us"] * 1e-6) / 1e9
-        c["frac"] = c["gbs"] / peak
-        if problems[j].kind == "moe_combine":
-            _, (ex, _, _), res_j, w_j, outs_j = sets[0][j]
-            v, thr = farn.farn_plan_moe_combine(
-                ctx.handle, problems[j].W, problems[j].T, problems[j].H, ex.data_ptr(),
-                res_j.data_ptr(), w_j.data_ptr(), outs_j[0].data_ptr(), outs_j[1].data_ptr(),
-                outs_j[2].data_ptr())
-            c["variant"] = ("combine-stage" if v == "stage" else v) + f" threads={thr}"
-            continue
-        v, cs, thr = farn.farn_plan_typed(ctx.handle, *plan_args(sets[0][j]))
-        c["variant"] = f"{v} cluster={cs} threads={thr}"
     dom = max(per_call, key=lambda c: c["kernel_us"] * c["count_per_step"])
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": measured_traffic(dom["call"], dom["variant"]),
                 "kernel_source_sha": kernel_source_sha(),
-                "kernel": kernel_name(dom["variant"]), "call": dom["call"],
+                "kernel": kernel_name(dom["variant"]), "plan": dom["variant"],
+                "call": dom["call"],
                 "algorithmic_bytes_per_launch": dom["bytes"],
-                "launch_us": dom["kernel_us"],
+                "launch_us": dom["kernel_us"], "launches_timed": dom["launches_timed"],
                 "peak_source": "measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)"
                 if peak_src == "measured" else "fallback 6.8 TB/s",
                 "timing": "CUDA events around a graph of back-to-back launches of this "
                           "call alone over its own rotating copies (> 2 x L2), right "
                           "after the timed steps"}
+    n_sets = runner.n_sets
+    head = config_summary(args.workload, problems, K, ms, step_stats, calib_ms, per_call,
+                          n_sets, set_bytes, l2, peak, world, clocks)
 
     # ---- end to end: pinned host inputs in, outputs back, every step
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(sets[0], problems, stream, dev, K, world, step_bytes)
+    del runner, sets
+    torch.cuda.empty_cache()
 
     cpu = cpu_baseline(problems, args.cpu_seconds) if (rank == 0 and world == 1) else None
+    head["cpu_baseline"] = cpu
+
+    # ---- every other benchmark configuration, in the same run
+    configs = {args.workload: head}
+    others = [] if args.only else [n for n in BENCH_CONFIGS if n != args.workload]
+    for name in others:
+        probs = load(name)
+        csets, cbytes = setup_sets(probs, dev, stream, l2, False)
+        crun = StepRunner(csets, ctx, stream, use_graph)
+        cK, cms, cstats, ccal, (c0, c1) = time_steps(
+            crun, stream, dev, None, max(3, args.warmup), world, target_ms=args.config_ms)
+        cper = time_calls_alone(probs, dev, ctx, l2)
+        annotate_calls(cper, probs, csets, ctx, peak)
+        cclk = sampler.summary(c0, c1) if sampler else None
+        summ = config_summary(name, probs, cK, cms, cstats, ccal, cper, crun.n_sets, cbytes,
+                              l2, peak, world, cclk)
+        summ["cpu_baseline"] = (cpu_baseline(probs, args.config_cpu_seconds)
+                                if (rank == 0 and world == 1) else None)
+        configs[name] = summ
+        del crun, csets
+        torch.cuda.empty_cache()
+    time.sleep(0.3 if sampler else 0)
+    if sampler:
+        sampler.stop()
 
     if rank == 0:
         line = {
@@ -537,11 +627,9 @@ def run_gpu(args):
                        "bytes_per_step": step_bytes,
                        "accumulate": "f32",
                        "residual_out": "in place over residual" if args.in_place else "separate",
-                       "l2": f"inputs rotated over {n_sets} device copies "
-                             f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x L2 {l2 / 1e6:.0f} MB); "
-                             "no flush",
-                       "launch": (f"CUDA graphs: one replay per rotation of {n_sets} "
-                                  "input copies, one-step graphs for the rest"
+                       "l2": head["l2"],
+                       "launch": (f"CUDA graphs: one replay per rotation of {n_sets} input "
+                                  "copies, one-step graphs for the rest"
                                   if use_graph else "direct launches"),
                        "calibration_ms_per_step": calib_ms,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -554,6 +642,11 @@ def run_gpu(args):
             "gpu_launches": K * len(problems),
             "clocks": clocks,
             "per_call": per_call,
+            "configs": configs,
+            "configs_note": ("every benchmark configuration measured in this run: the "
+                             "headline one with exactly --steps timed steps; each other one "
+                             f"with about {args.config_ms:g} ms of timed steps, then each "
+                             "call alone (per_call); each with its own oracle sample"),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -51,6 +51,7 @@ struct farn_ctx {
                          // [plain, FP8, MoE combine, NVFP4][4 vectors]
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
+  int fault_launch;    // FARN_FAULT_INJECT=launch at create: every launch fails
 };
 
 namespace {
@@ -510,8 +511,12 @@ int farn_check_args(const void* const* partials, int W, const void* residual,
 int farn_create(farn_ctx** out, int device) {
   if (!out || device < 0) return FARN_ERR_INVALID_ARG;
   *out = nullptr;
-  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "create") == 0)
-    return FARN_ERR_CUDA;
+  // Host-side fault injection for the tests, read here once: "create" fails
+  // this call, "launch" makes every launch of the new context fail (before
+  // anything is enqueued).  No per-call environment lookups.
+  const char* inject = getenv("FARN_FAULT_INJECT");
+  if (inject && strcmp(inject, "create") == 0) return FARN_ERR_CUDA;
+  const bool inject_launch = inject && strcmp(inject, "launch") == 0;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess) { cudaGetLastError(); return FARN_ERR_CUDA; }
   if (device >= ndev) return FARN_ERR_INVALID_ARG;
@@ -521,6 +526,7 @@ int farn_create(farn_ctx** out, int device) {
   farn_ctx* c = new (std::nothrow) farn_ctx;
   if (!c) return FARN_ERR_NOMEM;
   c->device = device;
+  c->fault_launch = inject_launch ? 1 : 0;
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
     delete c;
     cudaGetLastError();
@@ -760,8 +766,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
                          residual_out, norm_out, q_out, scale_out, qm, g);
   if (st != FARN_OK) return st;
   if (T == 0) return FARN_OK;
-  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
-    return FARN_ERR_CUDA;
+  if (ctx->fault_launch) return FARN_ERR_CUDA;
 
   Plan pl;
   st = make_plan(ctx, T, H,
@@ -900,8 +905,7 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
     const bool inplace_residual = (i == 1 && residual_out == residual);
     if (!inplace_residual && overlaps(outs[i], nb, residual, nb)) return FARN_ERR_ALIAS;
   }
-  if (getenv("FARN_FAULT_INJECT") && strcmp(getenv("FARN_FAULT_INJECT"), "launch") == 0)
-    return FARN_ERR_CUDA;
+  if (ctx->fault_launch) return FARN_ERR_CUDA;
 
   const bool vec_ok = H % 8 == 0 && aligned16(residual) && aligned16(weight) &&
                       aligned16(reduced_out) && aligned16(residual_out) &&

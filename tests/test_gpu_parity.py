@@ -389,22 +389,37 @@ def test_bad_eps_and_shapes_raise(dev):
 
 
 def test_injected_launch_fault_launches_nothing(dev):
+    """FARN_FAULT_INJECT=launch is read when the context is created (not on
+    every call): each launch of that context then fails on the host before
+    anything is enqueued, for the rank-sum path and the MoE combine alike."""
     W, T, H = 4, 8, 2048
     xs, res, w = _inputs(dev, W, T, H)
     outs = _sentinel_outputs(dev, T, H)
-    os.environ["FARN_FAULT_INJECT"] = "launch"
+    bad = make_ctx(FARN_FAULT_INJECT="launch")
     try:
         with pytest.raises(farn.FarnError) as e:
-            farn.forward(xs, res, w, 1e-6, out=outs)
+            farn.forward(xs, res, w, 1e-6, out=outs, ctx=bad)
+        assert e.value.status == farn.FARN_ERR_CUDA
+        pm = synth.Problem("moe", 2, T, H, 1e-6, 5, synth.N01, kind="moe_combine")
+        (ex, index, gates), mres, mw = synth.device_inputs(pm, dev)
+        with pytest.raises(farn.FarnError) as e:
+            farn.moe_combine(ex, index, gates, mres, mw, 1e-6, out=outs, ctx=bad)
         assert e.value.status == farn.FARN_ERR_CUDA
     finally:
-        os.environ.pop("FARN_FAULT_INJECT")
+        bad.close()
     torch.cuda.synchronize()
     for o in outs:
         assert np.all(u16(o) == SENTINEL)
-    # the context stays usable afterwards
-    farn.forward(xs, res, w, 1e-6, out=outs)
-    torch.cuda.synchronize()
+    # a context created without the variable is unaffected, even while it
+    # is set: the library does not look at it per call
+    good = farn.Context(0)
+    os.environ["FARN_FAULT_INJECT"] = "launch"
+    try:
+        farn.forward(xs, res, w, 1e-6, out=outs, ctx=good)
+    finally:
+        os.environ.pop("FARN_FAULT_INJECT")
+        torch.cuda.synchronize()
+        good.close()
     assert not np.all(u16(outs[2]) == SENTINEL)
 
 
