@@ -135,7 +135,7 @@ int farn_check_args(const void *const *partials, int W,
 /* Read and clear the context's device status word (blocking: waits for
  * the device).  0 means every wait of the TMA-staged kernel completed; a
  * non-zero value has one bit per kind of wait that gave up after its time
- * limit (2 s): 1 a consumer waiting for a staged row, 2 the producer
+ * limit (2 s): 1 a consumer waiting for a staged segment, 2 the producer
  * waiting for a free stage, 4 a consumer in the row reduction, 8 the
  * producer draining its copies.  The kernel that gave up left its outputs
  * incomplete.  Returns FARN_ERR_INVALID_ARG or FARN_ERR_CUDA on failure. */
@@ -150,9 +150,10 @@ const char *farn_status_string(int status);
 /* Which kernel variant farn_forward would launch for this shape and these
  * pointers, without launching: 0 row (one CTA per row), 1 cluster (a
  * cluster of CTAs splits each row), 2 generic (any H or alignment), 3 bulk
- * (persistent CTAs that stage rows in shared memory with TMA bulk copies),
- * 4 stage (persistent CTAs whose threads stage their own vectors in shared
- * memory with cp.async).
+ * (persistent CTAs whose producer warp stages column segments of every
+ * input row in shared memory with TMA bulk copies; rows of at most 16384
+ * elements), 4 stage (persistent CTAs whose threads stage their own
+ * vectors in shared memory with cp.async).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */
 int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,
@@ -175,8 +176,9 @@ int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,
  * memory beyond the caller's tensors is a 4-byte status word kept in a
  * fixed 256-byte array that this library places in every GPU's memory for
  * the life of the process; a call needs that one word whatever T, H and W
- * are.  Shapes the TMA-staged kernel does not take (tensors not 16-byte
- * aligned, H % 8 != 0, rows longer than 16384 elements) return
+ * are.  Every shape with 16-byte aligned tensors, H % 8 == 0 and
+ * H <= 16384 is taken, for any W <= FARN_MAX_W; other shapes (tensors not
+ * 16-byte aligned, H % 8 != 0, rows longer than 16384 elements) return
  * FARN_ERR_UNSUPPORTED.
  *
  * The first call on a device sets that device up (finds the array's device
@@ -278,10 +280,12 @@ int farn_moe_combine(const farn_ctx *ctx,
                      cudaStream_t stream);
 
 /* Which kernel farn_moe_combine would launch for this shape and these
- * pointers, without launching: 2 generic (any H or alignment), 4 stage
- * (persistent CTAs that gather the rows into shared memory with cp.async;
- * long inputs), 5 combine (one CTA per row).  *threads receives the threads
- * per CTA.  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
+ * pointers, without launching: 2 generic (any H or alignment), 3 bulk
+ * (persistent CTAs that gather the rows into shared memory with TMA bulk
+ * copies; chosen with FARN_BULK=1 or FARN_VARIANT=bulk at farn_create),
+ * 4 stage (persistent CTAs that gather the rows into shared memory with
+ * cp.async; long inputs), 5 combine (one CTA per row).  *threads receives
+ * the threads per CTA.  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
  * NULL pointer; aliasing is not checked). */
 int farn_plan_moe_combine(const farn_ctx *ctx, int K, int64_t T, int64_t H,
                           const void *expert_out, const void *residual,

@@ -108,13 +108,24 @@ VecKernel pick_generic(int pb) {
   return pb == 4 ? &farn::farn_generic_kernel<4> : &farn::farn_generic_kernel<2>;
 }
 
-VecKernel pick_bulk(int vpt) {
+// The bulk kernel instantiations: the most segments per row each takes.
+constexpr int kBulkVpts[5] = {1, 2, 4, 8, 16};
+
+template <bool COMBINE>
+VecKernel pick_bulk_t(int vpt) {
   switch (vpt) {
-    case 1: return &farn::farn_bulk_kernel<1>;
-    case 2: return &farn::farn_bulk_kernel<2>;
-    case 4: return &farn::farn_bulk_kernel<4>;
+    case 1: return &farn::farn_bulk_kernel<1, COMBINE>;
+    case 2: return &farn::farn_bulk_kernel<2, COMBINE>;
+    case 4: return &farn::farn_bulk_kernel<4, COMBINE>;
+    case 8: return &farn::farn_bulk_kernel<8, COMBINE>;
+    case 16: return &farn::farn_bulk_kernel<16, COMBINE>;
   }
   return nullptr;
+}
+
+// combine: the MoE combine's instantiation
+VecKernel pick_bulk(int vpt, bool combine = false) {
+  return combine ? pick_bulk_t<true>(vpt) : pick_bulk_t<false>(vpt);
 }
 
 struct Plan {
@@ -123,6 +134,7 @@ struct Plan {
   int cs;       // CTAs per row
   int vpt;      // vectors per thread
   int threads;  // threads per CTA
+  bool one_row; // row/cluster kernel: the one-row (latency-bound) instantiation
   int64_t grid;
   int stage_r;            // stage: chunks in flight per thread
   uint32_t stages;        // bulk: ring stages
@@ -130,34 +142,63 @@ struct Plan {
   size_t smem;            // bulk: dynamic shared memory bytes
 };
 
-// Bulk plan: one producer warp + enough consumer warps for the row at up to
-// 4 vectors per thread; a ring of as many row-sized stages as fit.
-bool make_bulk_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl) {
+// Bulk plan.  A row of hv vectors is cut into nseg segments of nct
+// vectors (nct consumer threads, a multiple of 32, at most 256); a ring
+// stage holds one segment of all W+1 inputs.  Chosen: the fewest segments
+// per row (fewest waits) whose ring holds at least 4 stages, else the
+// deepest ring of at least 2 stages; `ctas` resident CTAs per SM share the
+// SM's shared memory.  Rows longer than kBulkMaxH elements are not taken
+// (every shorter row is, for any W <= 32, at one CTA per SM: the longest
+// row at W = 32 takes 16 segments of 128 vectors and 3 stages).
+// force_vpt (FARN_VPT), when set, caps the segments per row.
+bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* pl) {
+  if (H > farn::kBulkMaxH) return false;
   const int64_t hv = H / 8;
-  int vpt = hv > 256 ? 4 : (hv > 128 ? 2 : 1);
-  if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
-  const int64_t nct = ((hv + vpt - 1) / vpt + 31) / 32 * 32;
-  const int bound = vpt >= 4 ? farn::BulkBounds<4>::kThreads
-                             : (vpt == 2 ? farn::BulkBounds<2>::kThreads
-                                         : farn::BulkBounds<1>::kThreads);
-  if (nct + 32 > bound || !pick_bulk(vpt)) return false;
-  const uint32_t stride = (uint32_t)((H * 2 + 127) / 128 * 128);
-  const size_t budget = (size_t)ctx->max_smem / (size_t)ctx->bulk_ctas;
+  const int max_seg = ctx->force_vpt > 0 ? ctx->force_vpt : 16;
+  const size_t budget = (size_t)ctx->max_smem / (size_t)ctas;
   const size_t fixed = sizeof(farn::BulkBarriers) + 128;
   if (budget <= fixed) return false;
-  size_t ns = (budget - fixed) / stride;
-  if (ns > farn::kBulkMaxStages) ns = farn::kBulkMaxStages;
-  if (ns < 4) return false;
+  int best_seg = 0, best_nct = 0;
+  size_t best_ns = 0;
+  uint32_t best_stride = 0;
+  for (int nseg = 1; nseg <= max_seg; ++nseg) {
+    const int64_t nct = ((hv + nseg - 1) / nseg + 31) / 32 * 32;
+    if (nct > farn::kBulkMaxConsumers) continue;
+    if ((hv + nct - 1) / nct != nseg) continue;   // the same split as fewer segments
+    const uint32_t stride = (uint32_t)((nct * 16 + 127) / 128 * 128);
+    size_t ns = (budget - fixed) / ((size_t)(W + 1) * stride);
+    if (ns > farn::kBulkMaxStages) ns = farn::kBulkMaxStages;
+    if (ns >= 4) { best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride; break; }
+    if (ns >= 2 && ns > best_ns) { best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride; }
+  }
+  if (!best_seg) return false;
+  int vpt = 0;
+  for (int v : kBulkVpts)
+    if (!vpt && v >= best_seg) vpt = v;
+  if (!vpt || !pick_bulk(vpt)) return false;
   pl->variant = kVariantBulk;
+  pl->pb = 2;
   pl->cs = 1;
+  pl->one_row = false;
   pl->vpt = vpt;
-  pl->threads = (int)nct + 32;
-  const int64_t resident = (int64_t)ctx->num_sms * ctx->bulk_ctas;
+  pl->threads = best_nct + 32;
+  const int64_t resident = (int64_t)ctx->num_sms * ctas;
   pl->grid = T < resident ? T : resident;
-  pl->stages = (uint32_t)ns;
-  pl->stage_stride = stride;
-  pl->smem = ns * stride + sizeof(farn::BulkBarriers);
+  pl->stages = (uint32_t)best_ns;
+  pl->stage_stride = best_stride;
+  pl->smem = best_ns * (size_t)(W + 1) * best_stride + sizeof(farn::BulkBarriers);
   return true;
+}
+
+// One resident CTA per SM unless FARN_BULK_CTAS=2 (then two where the
+// plan fits half the shared memory).  With the producer warp issuing a
+// segment's copies from W+1 lanes, one CTA per SM measured fastest on
+// GB300 (W = 4, T = 32768, H = 5120: 96.9 % of the copy bandwidth against
+// 89.5 % for two; W = 8, T = 8192, H = 8192: 97.0 % against 96.4 %; W = 16,
+// T = 4096, H = 7168: 98.7 % against 83.4 %).
+bool make_bulk_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, Plan* pl) {
+  if (ctx->bulk_ctas == 2 && bulk_fit(ctx, W, T, H, 2, pl)) return true;
+  return bulk_fit(ctx, W, T, H, 1, pl);
 }
 
 template <int VPT, int CS, int PB>
@@ -190,7 +231,21 @@ VecKernel pick_vec_pb(int vpt, int cs) {
   return nullptr;
 }
 
-VecKernel pick_vec(int vpt, int cs, int pb) {
+// The one-row instantiations (bf16 partials, one vector per thread) that
+// serve latency-bound calls.
+VecKernel pick_vec_one_row(int cs) {
+  switch (cs) {
+    case 1: return &farn::farn_vec_kernel<1, 1, 2, true>;
+    case 2: return &farn::farn_vec_kernel<1, 2, 2, true>;
+    case 4: return &farn::farn_vec_kernel<1, 4, 2, true>;
+    case 8: return &farn::farn_vec_kernel<1, 8, 2, true>;
+    case 16: return &farn::farn_vec_kernel<1, 16, 2, true>;
+  }
+  return nullptr;
+}
+
+VecKernel pick_vec(int vpt, int cs, int pb, bool one_row = false) {
+  if (one_row) return vpt == 1 && pb == 2 ? pick_vec_one_row(cs) : nullptr;
   return pb == 4 ? pick_vec_pb<4>(vpt, cs) : pick_vec_pb<2>(vpt, cs);
 }
 
@@ -254,6 +309,7 @@ bool stage_fit(const farn_ctx* ctx, int64_t hv, int vpt, int ctas, Plan* pl, int
   pl->variant = kVariantStage;
   pl->pb = 2;
   pl->cs = 1;
+  pl->one_row = false;
   pl->vpt = vpt;
   pl->threads = (int)nt;
   const int64_t resident = (int64_t)ctx->num_sms * ctas;
@@ -298,10 +354,11 @@ bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int ki
 }
 
 // in_bytes: the bytes the call reads (partials, residual, weight).
-int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
+int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int pb, Plan* out,
               int qm, int64_t in_bytes) {
   Plan pl;
   pl.pb = pb;
+  pl.one_row = false;
   const bool quant = qm != kQuantNone;
   // The FP8 and NVFP4 outputs are produced by every kernel but the
   // TMA-staged one.
@@ -312,7 +369,7 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
   pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
   if (vec_ok && pb == 2 && !quant && (want == kVariantBulk ||
                  (want == kVariantAuto && ctx->bulk && !small && ctx->force_cluster == 0)) &&
-      make_bulk_plan(ctx, T, H, &pl)) {
+      make_bulk_plan(ctx, W, T, H, &pl)) {
     *out = pl;
     return FARN_OK;
   }
@@ -371,6 +428,9 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
     pl.variant = cs > 1 ? kVariantCluster : kVariantRow;
     pl.cs = cs; pl.vpt = vpt; pl.threads = (int)threads;
     pl.grid = T * cs;
+    // latency-bound calls of one vector per thread: one CTA (or cluster)
+    // per row and no loop (T < small_t, so the grid is small)
+    pl.one_row = small && vpt == 1 && pb == 2;
   }
   // Grid limit: rows beyond one pass are looped over inside the kernel.
   const int64_t max_grid = (int64_t)0x7FFFFFFF / pl.cs * pl.cs;
@@ -390,9 +450,18 @@ int make_plan(const farn_ctx* ctx, int64_t T, int64_t H, bool vec_ok, int pb, Pl
 int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   pl.pb = 2; pl.cs = 1; pl.stages = 0; pl.stage_stride = 0; pl.smem = 0; pl.stage_r = 0;
+  pl.one_row = false;
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
-  if (want == kVariantCluster || want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
+  if (want == kVariantCluster) return FARN_ERR_UNSUPPORTED;
+  if (vec_ok && (want == kVariantBulk ||
+                 (want == kVariantAuto && ctx->bulk &&
+                  long_call(ctx, T, (int64_t)(K + 1) * T * H * 2))) &&
+      make_bulk_plan(ctx, K, T, H, &pl)) {
+    *out = pl;
+    return FARN_OK;
+  }
+  if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   if (vec_ok && want != kVariantGeneric && want != kVariantRow &&
       (want == kVariantStage || (ctx->stage && long_call(ctx, T, (int64_t)(K + 1) * T * H * 2))) &&
       make_stage_plan(ctx, T, H, &pl, 2)) {
@@ -540,9 +609,11 @@ int farn_create(farn_ctx** out, int device) {
     if (cudaFuncSetAttribute((const void*)k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       bool ok16 = true;
-      for (int i = 0; i < 6 && ok16; ++i) {
-        const int vpt = 1 << (i % 3), pb = i < 3 ? 2 : 4;
-        VecKernel k = pick_vec(vpt, 16, pb);
+      for (int i = 0; i < 7 && ok16; ++i) {
+        // the looping kernels (three vector counts, bf16 and fp32
+        // partials) and the one-row kernel
+        const int vpt = i < 6 ? 1 << (i % 3) : 1, pb = (i >= 3 && i < 6) ? 4 : 2;
+        VecKernel k = pick_vec(vpt, 16, pb, i == 6);
         if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) { ok16 = false; break; }
         cudaLaunchConfig_t cfg = {};
@@ -585,8 +656,8 @@ int farn_create(farn_ctx** out, int device) {
     cudaGetLastError();
     return FARN_ERR_CUDA;
   }
-  for (int vpt = 1; vpt <= 4; vpt *= 2) {
-    if (cudaFuncSetAttribute((const void*)pick_bulk(vpt),
+  for (int i = 0; i < 10; ++i) {
+    if (cudaFuncSetAttribute((const void*)pick_bulk(kBulkVpts[i % 5], i >= 5),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, c->max_smem) !=
         cudaSuccess) {
       delete c;
@@ -715,7 +786,7 @@ int farn_plan_typed(const farn_ctx* ctx, int partial_dtype, int flags, int W, in
   for (int r = 0; r < W; ++r)
     if (!partials[r]) return FARN_ERR_INVALID_ARG;
   Plan pl;
-  int st = make_plan(ctx, T, H,
+  int st = make_plan(ctx, W, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out ? norm_out : reduced_out, H),
                  pb, &pl, qm, (int64_t)W * T * H * pb + T * H * 2);
@@ -769,7 +840,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   if (ctx->fault_launch) return FARN_ERR_CUDA;
 
   Plan pl;
-  st = make_plan(ctx, T, H,
+  st = make_plan(ctx, W, T, H,
                  vector_path_ok(W, partials, residual, weight, reduced_out, residual_out,
                                 norm_out ? norm_out : reduced_out, H) &&
                      (qm != kQuantFp8 || ((uintptr_t)q_out & 15u) == 0) &&
@@ -840,7 +911,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   } else if (pl.variant == kVariantStage) {
     err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r, qm), prm);
   } else {
-    VecKernel k = pick_vec(pl.vpt, pl.cs, pb);
+    VecKernel k = pick_vec(pl.vpt, pl.cs, pb, pl.one_row);
     err = cudaLaunchKernelEx(&cfg, k, prm);
   }
   if (err != cudaSuccess) {
@@ -915,6 +986,7 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   if (st != FARN_OK) return st;
   const bool generic = pl.variant == kVariantGeneric;
   const bool staged = pl.variant == kVariantStage;
+  const bool bulk = pl.variant == kVariantBulk;
   farn::Params prm;
   memset(&prm, 0, sizeof prm);
   prm.residual = residual;
@@ -930,13 +1002,16 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   prm.index = index;
   prm.gates = gates;
   prm.n_slots = n_slots;
+  prm.err = ctx->d_status;
+  prm.stages = pl.stages;
+  prm.stage_stride = pl.stage_stride;
 
   DeviceGuard g(ctx->device);
   if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
   cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
-  cfg.dynamicSmemBytes = staged ? pl.smem : 0;
+  cfg.dynamicSmemBytes = (staged || bulk) ? pl.smem : 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -948,6 +1023,8 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
     err = cudaLaunchKernelEx(&cfg, farn::farn_generic_kernel<2, true>, prm);
   } else if (staged) {
     err = cudaLaunchKernelEx(&cfg, pick_combine_stage(pl.vpt, pl.stage_r), prm);
+  } else if (bulk) {
+    err = cudaLaunchKernelEx(&cfg, pick_bulk(pl.vpt, true), prm);
   } else {
     VecKernel k = pl.vpt == 1 ? &farn::farn_combine_kernel<1>
                   : (pl.vpt == 2 ? &farn::farn_combine_kernel<2> : &farn::farn_combine_kernel<4>);
@@ -975,9 +1052,9 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
 // The array is kNoAllocScratchBytes (256) bytes per GPU and every GPU that
 // loads this library holds it until the process exits.  A call uses its
 // first 4 bytes, whatever T, H and W are; the shapes this entry point takes
-// are those of the TMA-staged kernel (16-byte aligned tensors, H % 8 == 0,
-// rows of at most 16384 elements for W <= 32), others are refused with
-// FARN_ERR_UNSUPPORTED.
+// are those the TMA-staged kernel's plan takes: 16-byte aligned tensors,
+// H % 8 == 0 and H <= 16384 (kBulkMaxH), any W <= 32.
+// Others are refused with FARN_ERR_UNSUPPORTED.
 //
 // The array is shared by every call on the device and keeps the last
 // call's contents; each call clears the status word on its stream before
@@ -991,8 +1068,8 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 
 struct NoAllocDevice {
-  std::once_flag once;
-  int status = FARN_ERR_CUDA;   // result of the set-up
+  std::mutex mu;
+  bool ready = false;           // set-up done (a failed set-up is tried again)
   int* scratch = nullptr;       // device address of g_farn_noalloc_scratch
   int num_sms = 0;
   int max_smem = 0;
@@ -1003,9 +1080,9 @@ NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 // Once per device, with that device current: the scratch array's device
 // address (the array's name in host code is only a host-side stand-in),
 // the device limits and the bulk kernels' shared-memory attribute.
-void noalloc_setup(int device, NoAllocDevice* d) {
+int noalloc_setup(int device, NoAllocDevice* d) {
   DeviceGuard g(device);
-  if (!g.ok) { cudaGetLastError(); d->status = FARN_ERR_CUDA; return; }
+  if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }
   void* ptr = nullptr;
   if (cudaGetSymbolAddress(&ptr, g_farn_noalloc_scratch) != cudaSuccess || !ptr ||
       cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, device) !=
@@ -1013,20 +1090,18 @@ void noalloc_setup(int device, NoAllocDevice* d) {
       cudaDeviceGetAttribute(&d->max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
           cudaSuccess) {
     cudaGetLastError();
-    d->status = FARN_ERR_CUDA;
-    return;
+    return FARN_ERR_CUDA;
   }
-  for (int vpt = 1; vpt <= 4; vpt *= 2) {
+  for (int vpt : kBulkVpts) {
     if (cudaFuncSetAttribute((const void*)pick_bulk(vpt),
                              cudaFuncAttributeMaxDynamicSharedMemorySize, d->max_smem) !=
         cudaSuccess) {
       cudaGetLastError();
-      d->status = FARN_ERR_CUDA;
-      return;
+      return FARN_ERR_CUDA;
     }
   }
   d->scratch = static_cast<int*>(ptr);
-  d->status = FARN_OK;
+  return FARN_OK;
 }
 
 }  // namespace
@@ -1043,9 +1118,18 @@ int farn_forward_noalloc(int device, const void* const* partials, int W, const v
     if (status_out) *status_out = 0;
     return FARN_OK;
   }
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) { cudaGetLastError(); return FARN_ERR_CUDA; }
+  if (device >= ndev) return FARN_ERR_INVALID_ARG;
   NoAllocDevice* d = &g_noalloc_dev[device];
-  std::call_once(d->once, noalloc_setup, device, d);
-  if (d->status != FARN_OK) return d->status;
+  {
+    std::lock_guard<std::mutex> lock(d->mu);
+    if (!d->ready) {
+      st = noalloc_setup(device, d);
+      if (st != FARN_OK) return st;
+      d->ready = true;
+    }
+  }
   static_assert(sizeof(int) <= kNoAllocScratchBytes, "status word must fit the scratch array");
 
   if (!vector_path_ok(W, partials, residual, weight, reduced_out, residual_out, norm_out, H))
@@ -1060,7 +1144,7 @@ int farn_forward_noalloc(int device, const void* const* partials, int W, const v
   dc.bulk_ctas = 1;
   dc.force_variant = kVariantBulk;
   Plan pl;
-  if (!make_bulk_plan(&dc, T, H, &pl)) return FARN_ERR_UNSUPPORTED;
+  if (!make_bulk_plan(&dc, W, T, H, &pl)) return FARN_ERR_UNSUPPORTED;
 
   farn::Params prm;
   memset(&prm, 0, sizeof prm);

@@ -67,7 +67,7 @@ struct Params {
   // bulk (TMA-staged) kernel only
   int* err;               // device status word, bits of kBulkErr* on a timeout
   uint32_t stages;        // shared-memory ring stages
-  uint32_t stage_stride;  // bytes between stages (row bytes rounded to 128)
+  uint32_t stage_stride;  // bytes per input slot of a stage (multiple of 128)
 };
 
 // ----------------------------------------------------------- bf16 helpers
@@ -230,9 +230,11 @@ __device__ __forceinline__ void add8_x2(float* acc, uint4 v) {
 
 // acc[0..8) += g * f(v) for the eight bf16 values of one 16-byte vector,
 // the product and the sum each rounded to fp32 (__fmul_rn / __fadd_rn are
-// never fused into a multiply-add).  Measured alternatives: packed
-// mul.rn.f32x2 / add.rn.f32x2 did not keep the products separately
-// rounded; scalar products with packed sums were exact but no faster.
+// never fused into a multiply-add).  A packed form, mul.rn.f32x2 followed
+// by add.rn.f32x2 (explicit rounding on both), was measured against the
+// oracle on GB300 with this toolchain and did not reproduce separately
+// rounded products: 48 of 716,800 reduced values differed in a 32-expert
+// call.  Scalar products with packed sums were exact but no faster.
 __device__ __forceinline__ void gate_add8(float* acc, float g, uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -313,9 +315,14 @@ __device__ __forceinline__ float max_partials(const float* wm, int nw, int lane)
 // flight per thread per batch, plus the residual) and added in rank order.
 // PB is the partials' element size: 2 (bf16) or 4 (fp32, two 16-byte loads
 // per 8 elements); residual, weight and outputs are bf16 either way.  At
-// most 512 threads per CTA (128 registers per thread).
-template <int VPT, int CS, int PB = 2>
-__global__ void __launch_bounds__(512, 1)
+// most 512 threads per CTA (128 registers per thread); the one-vector bf16
+// instantiations are built for two CTAs of 512 threads per SM (64
+// registers), so that the next call's CTAs can start on an SM while this
+// call's CTA still runs there.  ONE_ROW (latency-bound calls, one CTA or
+// cluster per row, grid = T * CS): no loop over rows, which leaves the
+// registers to fetch the weight together with the partials.
+template <int VPT, int CS, int PB = 2, bool ONE_ROW = false>
+__global__ void __launch_bounds__(512, (VPT == 1 && PB == 2) ? 2 : 1)
 farn_vec_kernel(const __grid_constant__ Params p) {
   constexpr int PV = PB / 2;
   constexpr int G = (8 / (VPT * PV)) > 0 ? (8 / (VPT * PV)) : 1;
@@ -333,10 +340,12 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   __shared__ float cluster_mx[2][CS];
 
   const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
-  // Small slices (decode-sized calls) are latency bound: their weight is
-  // fetched up front, alongside the partials.  Larger ones fetch it after
-  // the rank loop, where it holds no registers during the loads.
-  constexpr bool kEarlyWeight = VPT <= 2;
+  // One-row calls and two vectors per thread: the weight is fetched up
+  // front, alongside the partials (latency-bound calls).  Otherwise it is
+  // fetched after the rank loop, where it holds no registers during the
+  // loads and its latency hides behind the row reduction (the looping
+  // one-vector build then fits 64 registers with no spill).
+  constexpr bool kEarlyWeight = VPT == 2 || ONE_ROW;
   uint4 wv[VPT];
 
   // Latency-bound calls (the host sets p.prefetch when there are fewer rows
@@ -367,6 +376,15 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   }
 
   pdl_wait();
+  // Latency-bound calls let the next kernel on the stream start launching
+  // as soon as this one is released: its CTAs then prefetch their rows into
+  // L2 during the whole of this call, one call ahead and no further (that
+  // kernel releases the one after it only once this one has finished).
+  // Measured on GB300 (W = 8, H = 4096, back-to-back calls): T = 64 from
+  // 2.62 to 2.28 us with two CTAs per SM, T = 128 from 3.35 to 2.87 us;
+  // triggering before the wait instead lets launches run many calls ahead
+  // and was slower (T = 64: 3.26 us).
+  if (p.prefetch) pdl_trigger();
   if (kEarlyWeight) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -377,7 +395,8 @@ farn_vec_kernel(const __grid_constant__ Params p) {
 
   const int64_t rows_per_pass = gridDim.x / CS;
   int it = 0;
-  for (int64_t row = blockIdx.x / CS; row < p.T; row += rows_per_pass, ++it) {
+  for (int64_t row = blockIdx.x / CS; row < p.T;
+       row = ONE_ROW ? p.T : row + rows_per_pass, ++it) {
     const int64_t base = row * hv + (int64_t)slice * sv;   // vector offset
 
     uint4 rv[VPT];
@@ -801,22 +820,33 @@ farn_combine_kernel(const __grid_constant__ Params p) {
 }
 
 // ------------------------------------------- bulk (TMA-staged) kernel
-// Persistent and warp-specialised.  Warp 0 is the producer: one thread
-// streams, row after row, the row of every partial x[0..W-1] and then the
-// row of the residual (W+1 contiguous chunks of H*2 bytes) into a ring of
-// shared-memory stages with cp.async.bulk (the TMA engine's bulk copy),
-// each completing on the stage's "full" mbarrier.  The other warps are the
-// consumers: they read their 16-byte vectors of each stage in rank order,
-// release the stage on its "empty" mbarrier, and run the same per-element
-// arithmetic and epilogue as farn_vec_kernel.  The ring keeps up to
-// stages * H * 2 bytes in flight per SM without holding registers.
+// Persistent and warp-specialised.  A row of hv 16-byte vectors is cut into
+// nseg column segments of at most nct vectors (nct = the consumer threads).
+// A stage of the shared-memory ring holds one segment of every input of a
+// row: W+1 slots (x[0..W-1], then the residual) of p.stage_stride bytes.
+// Warp 0 is the producer: one thread streams the segments of this CTA's
+// rows, in order, into the ring -- per segment one expect_tx on the stage's
+// "full" mbarrier and W+1 cp.async.bulk copies (the TMA engine's bulk copy)
+// completing on it.  The other warps are the consumers: thread c owns
+// vector c of every segment (vector k*nct + c of the row); per segment it
+// waits once for the stage, adds the W staged vectors in rank order, reads
+// the residual's, releases the stage (one arrival per warp on its "empty"
+// mbarrier) and rounds and stores reduced and residual_out; after the row's
+// last segment come the sum of squares and the normalisation, as in
+// farn_vec_kernel.  A row costs each consumer warp nseg waits, whatever W
+// is, and the ring keeps stages * (W+1) * stage_stride bytes in flight per
+// CTA without holding registers.
 //
 // Every wait is bounded: after kWaitLimitNs of globaltimer time the
 // waiting thread sets the CTA's abort flag and a bit in *p.err and
-// returns; the other threads see the flag in their own waits and leave;
-// the producer then waits (bounded again) for the copies it has in flight
-// before it exits, so no copy lands in a finished CTA's shared memory.
+// returns; the other threads see the flag in their own waits and leave.
+// The producer, once it has issued its last copy (or given up), always
+// waits (bounded again) for the copies it may still have in flight before
+// it exits, so no copy lands in the shared memory of a finished CTA.
 constexpr uint32_t kBulkMaxStages = 16;
+constexpr int kBulkMaxConsumers = 256;   // consumer threads per CTA
+constexpr int kBulkThreads = 32 + kBulkMaxConsumers;
+constexpr int64_t kBulkMaxH = 16384;     // longest row the bulk plan takes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr int kBulkErrFull = 1;     // consumer gave up waiting for a stage
 constexpr int kBulkErrEmpty = 2;    // producer gave up waiting for a free stage
@@ -878,7 +908,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   }
 }
 
-// Dynamic shared memory: [stages][stage_stride] ring, then the barriers.
+// Dynamic shared memory: [stages][W+1][stage_stride] ring, then the barriers.
 struct BulkBarriers {
   uint64_t full[kBulkMaxStages];
   uint64_t empty[kBulkMaxStages];
@@ -887,19 +917,25 @@ struct BulkBarriers {
   int abort_flag;
 };
 
-// Threads per CTA the bulk kernel is compiled for: one producer warp plus
-// up to 256 consumer threads at 4 vectors each, 512 at 2, 992 at 1.
-template <int VPT>
-struct BulkBounds {
-  static constexpr int kThreads = VPT >= 4 ? 288 : (VPT == 2 ? 544 : 1024);
-};
-
-template <int VPT>
-__global__ void __launch_bounds__(BulkBounds<VPT>::kThreads)
+// VPT: the most segments per row (vectors per consumer thread) this
+// instantiation takes.  The host guarantees H % 8 == 0, 16-byte aligned
+// tensors, ceil(hv / nct) <= VPT, a stage_stride of at least nct * 16 bytes
+// (a multiple of 128) and blockDim.x = 32 + nct with nct <= 256.
+// COMBINE: the MoE combine instead of the rank sum -- the W = K inputs of
+// a row are the gathered expert rows expert_out[index[t,k]], summed as
+// gates[t,k] * x with each product and sum rounded (slots outside
+// [0, n_slots) are neither copied nor added); the producer warp's lane k
+// and every consumer warp's lane k hold column k of the row's routing,
+// loaded one of the CTA's rows ahead.
+template <int VPT, bool COMBINE = false>
+__global__ void __launch_bounds__(kBulkThreads, 1)
 farn_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t NS = p.stages;
-  BulkBarriers* bb = reinterpret_cast<BulkBarriers*>(smem + (size_t)NS * p.stage_stride);
+  const uint32_t slot = p.stage_stride;
+  const int W = p.W;
+  const uint32_t stage_bytes = (uint32_t)(W + 1) * slot;
+  BulkBarriers* bb = reinterpret_cast<BulkBarriers*>(smem + (size_t)NS * stage_bytes);
   const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t full0 = (uint32_t)__cvta_generic_to_shared(&bb->full[0]);
   const uint32_t empty0 = (uint32_t)__cvta_generic_to_shared(&bb->empty[0]);
@@ -911,9 +947,16 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
   const int ncw = (int)(blockDim.x >> 5) - 1;          // consumer warps
   const int nct = ncw * 32;                            // consumer threads
   const int64_t hv = p.H >> 3;
-  const uint32_t row_bytes = (uint32_t)(p.H * 2);
-  const int W = p.W;
+  const int nseg = (int)((hv + nct - 1) / nct);        // segments per row
   const float Hf = (float)p.H;
+  // MoE routing column `lane` of row r (-1 / 0 past the last row or column)
+  auto load_slot = [&](int64_t r) -> int32_t {
+    return (r < p.T && lane < W) ? __ldg(p.index + r * W + lane) : -1;
+  };
+  auto load_gate = [&](int64_t r) -> float {
+    return (r < p.T && lane < W) ? __ldg(p.gates + r * W + lane) : 0.0f;
+  };
+  auto valid = [&](int32_t sl) { return sl >= 0 && (int64_t)sl < p.n_slots; };
 
   if (tid == 0) {
     for (uint32_t s = 0; s < NS; ++s) {
@@ -930,40 +973,79 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane != 0) return;
-    uint64_t q = 0;                       // chunks issued so far
+    // Lane 0 waits for a free stage and arms its "full" barrier; then lane
+    // r issues the copy of input r (and r + 32), so the W+1 copies of a
+    // segment are issued side by side rather than one after another.
+    uint64_t q = 0;                       // segments issued so far
     bool ok = true;
+    int32_t i_cur = -1, i_nxt = -1;       // MoE: this row's and the next row's slots
+    if constexpr (COMBINE) {
+      i_cur = load_slot(blockIdx.x);
+      i_nxt = load_slot(blockIdx.x + gridDim.x);
+    }
     for (int64_t row = blockIdx.x; row < p.T && ok; row += gridDim.x) {
-      const int64_t off = row * (int64_t)row_bytes;
-      for (int c = 0; c <= W; ++c, ++q) {
+      bool mine = false;                  // MoE: lane's slot is copied
+      uint32_t ncopy = (uint32_t)(W + 1);
+      if constexpr (COMBINE) {
+        mine = lane < W && valid(i_cur);
+        ncopy = (uint32_t)__popc(__ballot_sync(0xFFFFFFFFu, mine)) + 1;
+      }
+      for (int k = 0; k < nseg; ++k) {
         const uint32_t s = (uint32_t)(q % NS);
         const uint64_t n = q / NS;
-        if (n > 0 && !wait_phase(empty0 + 8 * s, (uint32_t)((n - 1) & 1), abort_flag, p.err,
-                                 kBulkErrEmpty)) {
+        int good = 1;
+        if (lane == 0 && n > 0)
+          good = wait_phase(empty0 + 8 * s, (uint32_t)((n - 1) & 1), abort_flag, p.err,
+                            kBulkErrEmpty) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, good, 0)) {
           ok = false;
           break;
         }
-        const unsigned char* src =
-            reinterpret_cast<const unsigned char*>(c < W ? p.x[c] : p.residual) + off;
-        mbar_arrive_expect_tx(full0 + 8 * s, row_bytes);
-        bulk_g2s(ring + s * p.stage_stride, src, row_bytes, full0 + 8 * s);
+        const int64_t v0 = (int64_t)k * nct;
+        const uint32_t bytes = (uint32_t)((hv - v0 < nct ? hv - v0 : nct) * 16);
+        const int64_t off = (row * hv + v0) * 16;
+        const uint32_t dst = ring + s * stage_bytes;
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * s, ncopy * bytes);
+        __syncwarp();
+        if constexpr (COMBINE) {
+          if (mine)
+            bulk_g2s(dst + (uint32_t)lane * slot,
+                     reinterpret_cast<const unsigned char*>(p.expert_out) +
+                         ((int64_t)i_cur * hv + v0) * 16,
+                     bytes, full0 + 8 * s);
+          if (lane == 0)
+            bulk_g2s(dst + (uint32_t)W * slot,
+                     reinterpret_cast<const unsigned char*>(p.residual) + off, bytes,
+                     full0 + 8 * s);
+        } else {
+          for (int r = lane; r <= W; r += 32)
+            bulk_g2s(dst + (uint32_t)r * slot,
+                     reinterpret_cast<const unsigned char*>(r < W ? p.x[r] : p.residual) + off,
+                     bytes, full0 + 8 * s);
+        }
+        ++q;
+      }
+      if constexpr (COMBINE) {
+        i_cur = i_nxt;
+        i_nxt = load_slot(row + 2 * (int64_t)gridDim.x);
       }
       if (row + gridDim.x >= p.T) pdl_trigger();
     }
-    if (!ok) {
-      // Drain: the last min(q, NS) chunks may still be in flight.
-      const uint64_t first = q > NS ? q - NS : 0;
-      for (uint64_t k = first; k < q; ++k) {
-        const uint32_t s = (uint32_t)(k % NS);
-        const uint32_t par = (uint32_t)((k / NS) & 1);
-        if (mbar_try_wait(full0 + 8 * s, par)) continue;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(full0 + 8 * s, par)) {
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(p.err, kBulkErrDrain);
-            break;
-          }
-        }
+    if (lane != 0) return;
+    // Drain, always: the last min(q, NS) segments may still be in flight
+    // (every earlier one was consumed before its stage was reused).
+    const uint64_t first = q > NS ? q - NS : 0;
+    for (uint64_t k = first; k < q; ++k) {
+      const uint32_t s = (uint32_t)(k % NS);
+      const uint32_t par = (uint32_t)((k / NS) & 1);
+      if (mbar_try_wait(full0 + 8 * s, par)) continue;
+      const uint64_t t0 = globaltimer_ns();
+      bool done = false;
+      while (!(done = mbar_try_wait(full0 + 8 * s, par)))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      if (!done) {
+        atomicOr(p.err, kBulkErrDrain);
+        break;
       }
     }
     return;
@@ -972,78 +1054,104 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
   // ------------------------------------------------------------ consumers
   const int ctid = tid - 32;
   const int cw = warp - 1;
-  uint4 wv[VPT];
+  // The weight slice stays in registers across rows (up to 8 segments);
+  // longer rows read it again per row (it stays cached).
+  constexpr bool kWeightRegs = VPT <= 8;
+  uint4 wv[kWeightRegs ? VPT : 1];
+  if constexpr (kWeightRegs) {
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int j = ctid + k * nct;
-    if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+    for (int k = 0; k < VPT; ++k) {
+      const int64_t j = (int64_t)k * nct + ctid;
+      if (k < nseg && j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+    }
   }
 
+  // MoE: this row's routing (c_*) and the CTA's next row's (n_*)
+  int32_t c_sl = -1, n_sl = -1;
+  float c_gt = 0.0f, n_gt = 0.0f;
+  if constexpr (COMBINE) {
+    c_sl = load_slot(blockIdx.x);
+    c_gt = load_gate(blockIdx.x);
+    n_sl = load_slot(blockIdx.x + gridDim.x);
+    n_gt = load_gate(blockIdx.x + gridDim.x);
+  }
   uint64_t q = 0;
   int it = 0;
   for (int64_t row = blockIdx.x; row < p.T; row += gridDim.x, ++it) {
     const int64_t base = row * hv;
-    float acc[VPT][8];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
-    uint4 rv[VPT];
-
-    // a1: rank sum from the staged rows, rank order; then the residual.
-    for (int c = 0; c <= W; ++c, ++q) {
-      const uint32_t s = (uint32_t)(q % NS);
-      if (!wait_phase(full0 + 8 * s, (uint32_t)((q / NS) & 1), abort_flag, p.err,
-                      kBulkErrFull))
-        return;
-      const uint32_t stage = ring + s * p.stage_stride;
-      uint4 v[VPT];
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const int j = ctid + k * nct;
-        v[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (j < hv) v[k] = ld_shared_v4(stage + 16u * (uint32_t)j);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      if (c < W) {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) add8(acc[k], v[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) rv[k] = v[k];
-      }
-    }
-    if (row + gridDim.x >= p.T) pdl_trigger();
-
-    // a2 + a5 and the thread's part of a3.
     uint4 ro[VPT];
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int j = ctid + k * nct;
-      if (j < hv) {
-        const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
-        uint32_t red[4], out[4];
+      if (k < nseg) {
+        const uint32_t s = (uint32_t)(q % NS);
+        if (!wait_phase(full0 + 8 * s, (uint32_t)((q / NS) & 1), abort_flag, p.err,
+                        kBulkErrFull))
+          return;
+        ++q;
+        const int64_t j = (int64_t)k * nct + ctid;
+        const bool in = j < hv;
+        // this thread's vector in slot r of the stage
+        const uint4* sv = reinterpret_cast<const uint4*>(smem + (size_t)s * stage_bytes) + ctid;
+        const int sstep = (int)(slot >> 4);
+        float acc[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          red[e] = pack_bf16x2(acc[k][2 * e], acc[k][2 * e + 1]);
-          const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
-          const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
-          out[e] = pack_bf16x2(s0, s1);
-          const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
-          ss = fmaf(q0, q0, ss);
-          ss = fmaf(q1, q1, ss);
+        for (int e = 0; e < 8; ++e) acc[e] = -0.0f;
+        uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (COMBINE) {
+          // gated sum of the gathered rows, k in order (the shuffles run on
+          // every lane; only the reads and adds depend on `in`)
+          for (int c = 0; c < W; ++c) {
+            const int32_t sl = __shfl_sync(0xFFFFFFFFu, c_sl, c);
+            const float g = __shfl_sync(0xFFFFFFFFu, c_gt, c);
+            if (in && valid(sl)) gate_add8(acc, g, sv[c * sstep]);
+          }
+          if (in) rv = sv[W * sstep];
+        } else if (in) {
+          // a1: rank order, four staged vectors read ahead of their adds
+          int r = 0;
+          for (; r + 4 <= W; r += 4) {
+            const uint4 v0 = sv[(r + 0) * sstep], v1 = sv[(r + 1) * sstep];
+            const uint4 v2 = sv[(r + 2) * sstep], v3 = sv[(r + 3) * sstep];
+            add8(acc, v0); add8(acc, v1); add8(acc, v2); add8(acc, v3);
+          }
+          for (; r < W; ++r) add8(acc, sv[r * sstep]);
+          rv = sv[W * sstep];
         }
-        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
-                  make_uint4(red[0], red[1], red[2], red[3]));
-        ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
-        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+        // the stage's values are in registers: release it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+        if (in) {
+          // a2 + a5 and the thread's part of a3
+          const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+          uint32_t red[4], out[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            red[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+            const float s0 = bf_lo(red[e]) + bf_lo(rw[e]);
+            const float s1 = bf_hi(red[e]) + bf_hi(rw[e]);
+            out[e] = pack_bf16x2(s0, s1);
+            const float q0 = bf_lo(out[e]), q1 = bf_hi(out[e]);
+            ss = fmaf(q0, q0, ss);
+            ss = fmaf(q1, q1, ss);
+          }
+          st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
+                    make_uint4(red[0], red[1], red[2], red[3]));
+          ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
+          st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+        }
       }
+    }
+    if (row + gridDim.x >= p.T) pdl_trigger();
+    if constexpr (COMBINE) {
+      c_sl = n_sl;
+      c_gt = n_gt;
+      n_sl = load_slot(row + 2 * (int64_t)gridDim.x);
+      n_gt = load_gate(row + 2 * (int64_t)gridDim.x);
     }
 
     // a3: consumer-warp sums through shared memory, one mbarrier per row
-    // parity (each consumer warp arrives once), summed in warp order.
+    // parity (each consumer warp arrives once), combined by a butterfly.
     ss = warp_sum(ss);
     const int par = it & 1;
     if (lane == 0) {
@@ -1053,17 +1161,19 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
     if (!wait_phase(reduce0 + 8 * par, (uint32_t)((it >> 1) & 1), abort_flag, p.err,
                     kBulkErrReduce))
       return;
-    float tot = 0.0f;
-    for (int w = 0; w < ncw; ++w) tot += bb->warp_ss[par][w];
+    const float tot = sum_partials(bb->warp_ss[par], ncw, lane);
 
     // a4
     const float rstd = 1.0f / sqrtf(tot / Hf + p.eps);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      const int j = ctid + k * nct;
-      if (j < hv) {
+      const int64_t j = (int64_t)k * nct + ctid;
+      if (k < nseg && j < hv) {
+        uint4 wk;
+        if constexpr (kWeightRegs) wk = wv[k];
+        else wk = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
         const uint32_t qv[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
-        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        const uint32_t w[4] = {wk.x, wk.y, wk.z, wk.w};
         uint32_t n[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -438,9 +438,10 @@ def pin_e4m3_rounding_vs_exact(O):
 def pin_e4m3_matches_torch_cast(O):
     """The library routine: torch's float8_e4m3fn cast (round to nearest
     even) agrees on finite values within range."""
-    torch = __import__("torch")
+    import pytest
+    torch = pytest.importorskip("torch")
     if not hasattr(torch, "float8_e4m3fn"):
-        return
+        pytest.skip("this torch has no float8_e4m3fn dtype: the library cross-check did not run")
     rng = np.random.default_rng(31)
     v = np.clip((rng.normal(size=4000) * np.exp2(rng.integers(-12, 9, 4000))), -448, 448)
     v = v.astype(np.float32)

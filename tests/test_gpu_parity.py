@@ -121,15 +121,24 @@ def test_forced_variants_match_oracle_and_each_other(O, dev, env, shape):
 
 
 @pytest.mark.parametrize("name,T", [("prefill", 1000), ("nonpow2", 613), ("wide", 300),
-                                    ("decode", 4096), ("c1", 777), ("small_h", 999)])
+                                    ("decode", 4096), ("c1", 777), ("small_h", 999),
+                                    ("ragged", 401), ("w32_h16384", 40), ("w4_h16384", 333),
+                                    ("tiny_h", 157)])
 def test_bulk_variant(O, dev, name, T):
     """The TMA-staged persistent kernel on the five shapes' H, W and value
     recipes; T larger than the resident grid, so CTAs loop over rows and
-    the shared-memory ring wraps many times."""
+    the shared-memory ring wraps many times.  Also: a row whose last
+    segment is shorter than the others (H = 5128: 641 vectors in segments
+    of 224), the longest row at the most partials (W = 32, H = 16384: 16
+    segments, a 3-stage ring), the longest row at few partials, and rows
+    shorter than one warp of vectors."""
     ctx = make_ctx(FARN_VARIANT="bulk")
     try:
-        if name == "small_h":         # H = 1024: one vector per consumer thread
-            p = synth.Problem("small_h", 5, T, 1024, 1e-6, 9, synth.N01)
+        shapes = {"small_h": (5, 1024), "ragged": (6, 5128), "w32_h16384": (32, 16384),
+                  "w4_h16384": (4, 16384), "tiny_h": (3, 48)}
+        if name in shapes:
+            W, H = shapes[name]
+            p = synth.Problem(name, W, T, H, 1e-6, 9, synth.N01)
         else:
             p = synth.workload(name)[0].with_T(T)
         xs, res, w = synth.device_inputs(p, dev)
@@ -142,6 +151,23 @@ def test_bulk_variant(O, dev, name, T):
         assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, p.eps),
                       f"bulk {name} T={T}")
         assert farn.farn_device_status(ctx.handle) == 0
+    finally:
+        ctx.close()
+
+
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_bulk_variant_ctas_per_sm(O, dev, ctas):
+    """One or two resident TMA-staged CTAs per SM (FARN_BULK_CTAS)."""
+    ctx = make_ctx(FARN_VARIANT="bulk", FARN_BULK_CTAS=ctas)
+    try:
+        for name, T in (("prefill", 700), ("wide", 500), ("nonpow2", 900)):
+            p = synth.workload(name)[0].with_T(T)
+            xs, res, w = synth.device_inputs(p, dev)
+            out = farn.forward(xs, res, w, p.eps, ctx=ctx)
+            torch.cuda.synchronize()
+            assert_parity([u16(o) for o in out], oracle_rows(O, xs, res, w, p.eps),
+                          f"bulk x{ctas} {name}")
+            assert farn.farn_device_status(ctx.handle) == 0
     finally:
         ctx.close()
 
@@ -468,12 +494,21 @@ def test_dependent_chain(O, dev, pdl):
 
 
 def test_bulk_forced_on_unsupported_shape_is_an_error(dev):
-    """Forcing the TMA-staged kernel where its consumer warps cannot cover
-    the row (at 4 vectors per thread, more than 256 consumer threads) is
-    refused, not mis-run."""
+    """Forcing the TMA-staged kernel where it cannot cover the row is
+    refused, not mis-run: at most 4 segments per row (FARN_VPT=4) of at
+    most 256 vectors cannot hold 12288 elements, and no plan takes rows
+    longer than 16384 elements."""
     ctx = make_ctx(FARN_VARIANT="bulk", FARN_VPT=4)
     try:
         xs, res, w = _inputs(dev, 4, 8, 12288)
+        with pytest.raises(farn.FarnError) as e:
+            farn.forward(xs, res, w, 1e-6, ctx=ctx)
+        assert e.value.status == farn.FARN_ERR_UNSUPPORTED
+    finally:
+        ctx.close()
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        xs, res, w = _inputs(dev, 2, 4, 16392)
         with pytest.raises(farn.FarnError) as e:
             farn.forward(xs, res, w, 1e-6, ctx=ctx)
         assert e.value.status == farn.FARN_ERR_UNSUPPORTED
@@ -686,7 +721,7 @@ def test_cuda_graph_quantised_and_moe(O, dev):
                 assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"replay {k}"
 
 
-@pytest.mark.parametrize("variant", ["auto", "stage", "row"])
+@pytest.mark.parametrize("variant", ["auto", "stage", "row", "bulk"])
 def test_moe_combine_32_experts(O, dev, variant):
     """K = 32 (every lane of the routing registers in use), many rows per
     persistent CTA."""
@@ -867,7 +902,9 @@ def test_moe_combine_full_size_sampled(O, dev):
 @pytest.mark.parametrize("env", [dict(FARN_VARIANT="generic"), dict(FARN_VPT=1),
                                  dict(FARN_VPT=2), dict(FARN_VPT=4), dict(FARN_VARIANT="stage"),
                                  dict(FARN_VARIANT="stage", FARN_VPT=2),
-                                 dict(FARN_VARIANT="stage", FARN_STAGE_CTAS=1)],
+                                 dict(FARN_VARIANT="stage", FARN_STAGE_CTAS=1),
+                                 dict(FARN_VARIANT="bulk"), dict(FARN_VARIANT="bulk", FARN_BULK_CTAS=1),
+                                 dict(FARN_VARIANT="bulk", FARN_BULK_CTAS=2)],
                          ids=lambda e: "-".join(f"{k[5:].lower()}{v}" for k, v in e.items()))
 def test_moe_combine_variants(O, dev, env):
     ctx = make_ctx(**env)
@@ -877,7 +914,7 @@ def test_moe_combine_variants(O, dev, env):
         ctx.close()
 
 
-@pytest.mark.parametrize("variant", ["row", "stage"])
+@pytest.mark.parametrize("variant", ["row", "stage", "bulk"])
 def test_moe_combine_skipped_and_bad_slots(O, dev, variant):
     """-1 and out-of-range slots are skipped (never read); a token with no
     valid slot gets reduced = -0."""
@@ -896,7 +933,7 @@ def test_moe_combine_skipped_and_bad_slots(O, dev, variant):
         ctx.close()
 
 
-@pytest.mark.parametrize("variant", ["auto", "stage"])
+@pytest.mark.parametrize("variant", ["auto", "stage", "bulk"])
 def test_moe_combine_mid_size(O, dev, variant):
     """Many rows per persistent CTA for the staged gather kernel."""
     ctx = make_ctx(FARN_VARIANT=variant)
@@ -927,7 +964,9 @@ def test_moe_combine_plan(dev):
             assert v == "generic"
             for env, want_v in ((dict(FARN_VARIANT="row"), "combine"),
                                 (dict(FARN_VARIANT="generic"), "generic"),
-                                (dict(FARN_STAGE=0), "combine")):
+                                (dict(FARN_STAGE=0), "combine"),
+                                (dict(FARN_VARIANT="bulk"), "bulk"),
+                                (dict(FARN_BULK=1), "bulk")):
                 ctx = make_ctx(**env)
                 try:
                     v, _ = farn.farn_plan_moe_combine(ctx.handle, 8, T, p.H, ex.data_ptr(),
