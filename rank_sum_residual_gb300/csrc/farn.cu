@@ -267,7 +267,7 @@ int env_int(const char* name, int dflt) {
 // takes at most 512 threads, so slices of up to 2048 vectors, H <= 16384
 // for one CTA per row).
 // Below this many rows a latency-bound call splits rows over a cluster.
-constexpr int64_t kClusterRowsMax = 8;
+constexpr int64_t kClusterRowsMax = 16;
 
 int choose_vpt(int64_t sv) {
   if (sv >= 512) return 4;
@@ -391,17 +391,21 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
     int cs = 1;
     if (ctx->force_cluster > 0 && want != kVariantRow) {
       cs = ctx->force_cluster;
-    } else if (want != kVariantRow && small && T < kClusterRowsMax && hv > 512) {
-      // A handful of long rows: split each row over a cluster so that every
-      // CTA owns about 64 16-byte vectors and each thread one vector of
-      // every rank, spreading the row's loads over up to 8 SMs.  Rows of
-      // up to 512 vectors (H <= 4096) stay in one CTA of one vector per
-      // thread: with the L2 prefetch before the wait that measured faster
-      // on GB300 (T = 1, 2, 4 at H = 4096: 2.63 us against 2.70-2.73 us for
-      // the 8-CTA split; from 8 rows one CTA per row was already as fast).
+    } else if (want != kVariantRow && small &&
+               (pb == 2 ? (T < kClusterRowsMax && hv >= 256) : (T < 8 && hv > 512))) {
+      // A handful of rows: split each row over a cluster so that every CTA
+      // owns about 128 16-byte vectors (bf16 partials) and each thread one
+      // vector of every rank, spreading the row's loads over up to 8 SMs.
+      // Measured on GB300 (W = 8, H = 4096, back-to-back calls,
+      // reduced/residual_out stored after the DSMEM exchange): 4-CTA
+      // clusters 1.78 / 1.90 us at T = 1 / 8 against 1.91 / 2.07 us for one
+      // CTA per row; at T = 32 and above one CTA per row is faster.  fp32
+      // partials keep the earlier rule: rows longer than 4096 elements
+      // below 8 rows, about 64 vectors per CTA.
       const int cap = ctx->max_cluster < 8 ? ctx->max_cluster : 8;
+      const int64_t min_slice = pb == 2 ? 128 : 64;
       // (The NVFP4 output pairs vectors 2m, 2m+1 inside a CTA: even slices.)
-      while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= 64 &&
+      while (cs * 2 <= cap && hv % (cs * 2) == 0 && hv / (cs * 2) >= min_slice &&
              (qm != kQuantNvfp4 || (hv / (cs * 2)) % 2 == 0))
         cs *= 2;
     }

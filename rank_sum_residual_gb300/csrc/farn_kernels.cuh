@@ -27,6 +27,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace farn {
 
 constexpr int kMaxW = 32;
@@ -409,8 +411,14 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
     }
 
-    // a1: rank sum in fp32, rank order 0..W-1.
-    for (int r0 = 0; r0 < p.W; r0 += G) {
+    // a1: rank sum in fp32, rank order 0..W-1, G ranks per batch of loads.
+    // The first batch names its partials by constant rank indices (x[g]
+    // straight from the parameter bank); later batches index the pointer
+    // array at run time.  Measured on GB300 (W = 8, H = 4096, T = 64,
+    // back-to-back calls): 2.86 us with every batch indexed at run time,
+    // 2.40 us with the first batch constant.
+    auto batch = [&](auto first, int r0_run) {
+      const int r0 = decltype(first)::value ? 0 : r0_run;
       uint4 xv[G][VPT][PV];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -436,11 +444,18 @@ farn_vec_kernel(const __grid_constant__ Params p) {
           }
         }
       }
-    }
+    };
+    batch(std::true_type(), 0);
+    for (int r0 = G; r0 < p.W; r0 += G) batch(std::false_type(), r0);
 
     // a2 + a5: reduced and residual_out, rounded and stored; a3: the
     // thread's part of the sum of squares of the rounded residual_out.
-    uint4 ro[VPT];
+    // In a one-row cluster the two stores wait until after the DSMEM
+    // exchange below: its release would otherwise wait for them to reach
+    // memory (measured on GB300, 4-CTA clusters at T = 1..8, H = 4096:
+    // about 0.3 us per call).
+    constexpr bool kLateStores = CS > 1 && ONE_ROW;
+    uint4 ro[VPT], rd[VPT];
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -458,10 +473,12 @@ farn_vec_kernel(const __grid_constant__ Params p) {
           ss = fmaf(q0, q0, ss);
           ss = fmaf(q1, q1, ss);
         }
-        st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j,
-                  make_uint4(red[0], red[1], red[2], red[3]));
+        rd[k] = make_uint4(red[0], red[1], red[2], red[3]);
         ro[k] = make_uint4(out[0], out[1], out[2], out[3]);
-        st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+        if (!kLateStores) {
+          st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j, rd[k]);
+          st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+        }
       }
     }
 
@@ -501,6 +518,14 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       tot = 0.0f;
 #pragma unroll
       for (int c = 0; c < CS; ++c) tot += slots[c];
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * blockDim.x;
+        if (kLateStores && j < sv) {
+          st_stream(reinterpret_cast<uint4*>(p.reduced) + base + j, rd[k]);
+          st_stream(reinterpret_cast<uint4*>(p.residual_out) + base + j, ro[k]);
+        }
+      }
     }
 
     // a4: rstd with IEEE division and square root, then the normalised,

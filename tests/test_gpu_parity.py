@@ -250,9 +250,11 @@ def test_plan_choices(dev):
         assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
         assert plan(8, 1023, 8192)[0] == "row"
         assert plan(4, 1024, 5120)[0] == "row"          # 52 MB
-        assert plan(8, 1, 4096) == ("row", 1, 512)     # one CTA of 512 threads
-        assert plan(8, 1, 8192)[0] == "cluster"         # longer rows: split
-        assert plan(8, 1, 8192)[1] == 8
+        assert plan(8, 1, 4096) == ("cluster", 4, 128)  # few rows: 128 vectors per CTA
+        assert plan(8, 8, 4096) == ("cluster", 4, 128)
+        assert plan(8, 1, 8192) == ("cluster", 8, 128)  # longer rows: wider split
+        assert plan(8, 1, 1024) == ("row", 1, 128)      # short rows stay in one CTA
+        assert plan(8, 16, 4096) == ("row", 1, 512)     # from 16 rows: one CTA per row
         assert plan(8, 64, 4096) == ("row", 1, 512)     # decode: all ranks at once
         assert plan(4, 16, 13)[0] == "generic"          # H % 8 != 0
         assert plan(4, 16, 2048, off=2)[0] == "generic"  # misaligned
