@@ -632,6 +632,11 @@ def run_gpu(args):
                                   "copies, one-step graphs for the rest"
                                   if use_graph else "direct launches"),
                        "calibration_ms_per_step": calib_ms,
+                       "timing": (f"exactly {K} back-to-back steps after {args.warmup} "
+                                  "warm-up steps, CUDA events on the launching stream; "
+                                  "the spread over chunks of them is step_ms_spread; "
+                                  f"roofline.launch_us from {roofline['launches_timed']} "
+                                  "launches of the call alone"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "rows_per_s": rows_per_s,
             "pct_hbm_peak": 100.0 * value / world / peak,
