@@ -379,21 +379,23 @@ def setup_sets(problems, dev, stream, l2, in_place):
 
 class StepRunner:
     """Steps of one workload over its rotating input copies.  One CUDA graph
-    replay is one rotation (n_sets steps), plus a one-step graph per copy,
-    so exactly the requested number of steps is run and the host never
-    paces the GPU."""
+    replay covers whole rotations, at least `min_block` steps (block steps),
+    plus a one-step graph per copy, so exactly the requested number of
+    steps is run, the host never paces the GPU, and few replay boundaries
+    fall inside a short timed region."""
 
-    def __init__(self, sets, ctx, stream, use_graph):
+    def __init__(self, sets, ctx, stream, use_graph, min_block=10):
         import torch
         self.sets, self.ctx, self.stream = sets, ctx, stream
         self.n_sets = len(sets)
+        self.block = self.n_sets * max(1, -(-min_block // self.n_sets))
         self.use_graph = use_graph
         self.graph, self.step_graphs, self.pos = None, [], 0
         if use_graph:
             self.graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(self.graph, stream=stream):
-                for k in range(self.n_sets):
-                    self.step(k)
+                for k in range(self.block):
+                    self.step(k % self.n_sets)
             for k in range(self.n_sets):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
@@ -411,9 +413,9 @@ class StepRunner:
     def run(self, n):
         """Exactly n steps, continuing the rotation over the input copies."""
         while n > 0:
-            if self.use_graph and self.pos == 0 and n >= self.n_sets:
+            if self.use_graph and self.pos == 0 and n >= self.block:
                 self.graph.replay()
-                n -= self.n_sets
+                n -= self.block
                 continue
             if self.use_graph:
                 self.step_graphs[self.pos].replay()
@@ -441,12 +443,18 @@ def time_steps(runner, stream, dev, K, warmup, world, target_ms=1500.0):
         K = max(20, int(target_ms / max(calib_ms, 1e-4)))
         K = (K + n_sets - 1) // n_sets * n_sets
     runner.run(warmup)
+    if runner.pos:
+        # untimed steps up to the next whole rotation, so that the timed
+        # steps start on a block graph
+        runner.run(runner.n_sets - runner.pos)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     # The K steps run back to back; events between consecutive chunks of
     # them (recorded on the same stream, no gap added) give the spread.
-    n_chunks = max(1, min(20, K))
+    # Chunks are whole graph blocks where K allows, so that short timed
+    # regions do not replay one-step graphs.
+    n_chunks = max(1, min(20, K // runner.block if K >= runner.block else 1))
     bounds = [round(K * i / n_chunks) for i in range(n_chunks + 1)]
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
     t_wall0 = time.time()
@@ -579,7 +587,7 @@ def run_gpu(args):
                 "timing": "CUDA events around a graph of back-to-back launches of this "
                           "call alone over its own rotating copies (> 2 x L2), right "
                           "after the timed steps"}
-    n_sets = runner.n_sets
+    n_sets, block = runner.n_sets, runner.block
     head = config_summary(args.workload, problems, K, ms, step_stats, calib_ms, per_call,
                           n_sets, set_bytes, l2, peak, world, clocks)
 
@@ -628,9 +636,9 @@ def run_gpu(args):
                        "accumulate": "f32",
                        "residual_out": "in place over residual" if args.in_place else "separate",
                        "l2": head["l2"],
-                       "launch": (f"CUDA graphs: one replay per rotation of {n_sets} input "
-                                  "copies, one-step graphs for the rest"
-                                  if use_graph else "direct launches"),
+                       "launch": (f"CUDA graphs: one replay per {block} steps (whole "
+                                  f"rotations of {n_sets} input copies), one-step graphs "
+                                  "for the rest" if use_graph else "direct launches"),
                        "calibration_ms_per_step": calib_ms,
                        "timing": (f"exactly {K} back-to-back steps after {args.warmup} "
                                   "warm-up steps, CUDA events on the launching stream; "

@@ -120,6 +120,32 @@ def test_forced_variants_match_oracle_and_each_other(O, dev, env, shape):
         ctx.close()
 
 
+@pytest.mark.parametrize("W,T,H,plan", [
+    (32, 5, 4096, ("cluster", 4, 128)),   # four batches of partials, cluster split
+    (9, 40, 4096, ("row", 1, 512)),       # one full batch and one partial
+    (32, 100, 2048, ("row", 1, 256)),
+    (12, 1, 8192, ("cluster", 8, 128)),
+    (1, 7, 4096, ("cluster", 4, 128)),    # one partial: residual add + RMSNorm
+    (3, 151, 4096, ("row", 1, 512)),      # the last latency-bound row count
+], ids=lambda v: str(v).replace(" ", ""))
+def test_one_row_decode_builds(O, dev, W, T, H, plan):
+    """The one-row builds that serve latency-bound calls (first batch of
+    partial pointers by constant rank index, later batches at run time;
+    one-row clusters store reduced/residual_out after the DSMEM exchange)
+    against the oracle, in full."""
+    p = synth.Problem("onerow", W, T, H, 1e-5, 21 + W, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    outs = [torch.empty_like(res) for _ in range(3)]
+    c = farn._context_for(0)
+    got_plan = farn.farn_plan(c.handle, W, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                              w.data_ptr(), *[o.data_ptr() for o in outs])
+    assert got_plan == plan
+    farn.forward(xs, res, w, p.eps, out=outs)
+    torch.cuda.synchronize()
+    assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, p.eps),
+                  f"one-row build W={W} T={T} H={H}")
+
+
 @pytest.mark.parametrize("name,T", [("prefill", 1000), ("nonpow2", 613), ("wide", 300),
                                     ("decode", 4096), ("c1", 777), ("small_h", 999),
                                     ("ragged", 401), ("w32_h16384", 40), ("w4_h16384", 333),
