@@ -95,3 +95,24 @@ def test_clock_summary_filters_the_timed_region():
     assert s["samples"] == 2 and s["sm_mhz"] == 2065.0 and s["reasons"] == ["sw_power_cap"]
     s = c.summary(2.1, 2.2)                 # nothing inside: nearest samples
     assert s["samples"] > 0 and "nearest" in s["note"]
+
+
+def test_bars_and_config_summary():
+    """The acceptance bars on the fraction of the HBM roofline (75 % for
+    T >= 4096, 40 % for T <= 128, none in between) and the per-configuration
+    summary bench.py adds to its JSON line."""
+    assert bench.bar_for(4096) == 0.75 and bench.bar_for(32768) == 0.75
+    assert bench.bar_for(128) == 0.40 and bench.bar_for(1) == 0.40
+    assert bench.bar_for(129) is None and bench.bar_for(4095) is None
+    probs = synth.workload("decode")[-2:]          # T = 64 and 128
+    per_call = [dict(call=p.name, T=p.T, W=p.W, H=p.H, bytes=p.algorithmic_bytes(),
+                     kernel_us=t, frac=f) for p, t, f in zip(probs, (2.5, 3.1), (0.37, 0.6))]
+    s = bench.config_summary("decode", probs, K=10, ms=0.056, stats={}, calib_ms=0.0056,
+                             per_call=per_call, n_sets=3, set_bytes=10 ** 8, l2=10 ** 8,
+                             peak=6800.0, world=1, clocks=None)
+    step_bytes = sum(p.algorithmic_bytes() for p in probs)
+    assert s["bytes_per_step"] == step_bytes and s["rows_per_step"] == 192
+    assert abs(s["gbs"] - step_bytes * 10 / 0.056e-3 / 1e9) < 1e-6
+    assert abs(s["frac"] - s["gbs"] / 6800.0) < 1e-12
+    assert s["bar"]["decode@T64"] == {"target_frac": 0.40, "frac": 0.37, "met": False}
+    assert s["bar"]["decode@T128"]["met"] is True
