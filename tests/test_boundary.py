@@ -177,3 +177,26 @@ def test_synth_moe_routing():
     assert np.array_equal(index, i2) and np.array_equal(gates, g2)
     i3, _ = synth.moe_routing(p.with_seed(p.seed + 1))
     assert not np.array_equal(index, i3)
+
+
+def test_noalloc_host_side_checks():
+    """farn_forward_noalloc's argument checks and the empty call need no
+    GPU: T = 0 returns FARN_OK with a zero status word and launches nothing
+    (null data pointers allowed, as for empty tensors); bad arguments and a
+    negative device are refused before any CUDA call."""
+    a = 1 << 40
+    st, word = farn.farn_forward_noalloc(0, [0, 0], 2, 0, 0, 1e-6, 0, 4096, 0, 0, 0,
+                                         want_status=True)
+    assert st == farn.FARN_OK and word == 0
+    st, _ = farn.farn_forward_noalloc(0, [a], 0, a, a, 1e-6, 4, 4096, a, a, a)
+    assert st == farn.FARN_ERR_INVALID_ARG                      # W = 0
+    st, _ = farn.farn_forward_noalloc(0, [a] * 33, 33, a, a, 1e-6, 4, 4096, a, a, a)
+    assert st == farn.FARN_ERR_INVALID_ARG                      # W > FARN_MAX_W
+    st, _ = farn.farn_forward_noalloc(0, [a], 1, a, a, float("nan"), 4, 4096, a, a, a)
+    assert st == farn.FARN_ERR_INVALID_ARG                      # eps not finite
+    st, _ = farn.farn_forward_noalloc(-1, [a], 1, a, a, 1e-6, 4, 4096, a, a, a)
+    assert st == farn.FARN_ERR_INVALID_ARG                      # no such device
+    g = 1 << 32
+    st, _ = farn.farn_forward_noalloc(0, [a], 1, a + g, a + 2 * g, 1e-6, 4, 4096,
+                                      a, a + 3 * g, a + 4 * g)
+    assert st == farn.FARN_ERR_ALIAS                            # reduced_out over x[0]
