@@ -1264,11 +1264,18 @@ farn_stage_kernel(const __grid_constant__ Params p) {
   };
 
   pdl_wait();
-  uint4 wv[VPT];
+  // The weight slice stays in registers across rows, except in the FP8
+  // build (64 registers for two CTAs of 512 threads per SM, where the
+  // previous row's values are held for its pipelined amax): there it is
+  // read again for every row from cache, which removes a register spill.
+  constexpr bool kWeightRegs = QM != 1;
+  uint4 wv[kWeightRegs ? VPT : 1];
+  if constexpr (kWeightRegs) {
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int j = tid + k * nt;
-    if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * nt;
+      if (j < hv) wv[k] = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
+    }
   }
 
   // Chunk cursor for issuing: (row, c); chunks run over this CTA's rows.
@@ -1413,8 +1420,11 @@ farn_stage_kernel(const __grid_constant__ Params p) {
     for (int k = 0; k < VPT; ++k) {
       const int j = tid + k * nt;
       if (j < hv) {
+        uint4 wk;
+        if constexpr (kWeightRegs) wk = wv[k];
+        else wk = ld_keep(reinterpret_cast<const uint4*>(p.weight) + j);
         const uint32_t qv[4] = {ro[k].x, ro[k].y, ro[k].z, ro[k].w};
-        const uint32_t w[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        const uint32_t w[4] = {wk.x, wk.y, wk.z, wk.w};
         uint32_t n[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
