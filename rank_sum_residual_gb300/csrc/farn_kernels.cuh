@@ -233,10 +233,14 @@ __device__ __forceinline__ void add8_x2(float* acc, uint4 v) {
 // acc[0..8) += g * f(v) for the eight bf16 values of one 16-byte vector,
 // the product and the sum each rounded to fp32 (__fmul_rn / __fadd_rn are
 // never fused into a multiply-add).  A packed form, mul.rn.f32x2 followed
-// by add.rn.f32x2 (explicit rounding on both), was measured against the
-// oracle on GB300 with this toolchain and did not reproduce separately
-// rounded products: 48 of 716,800 reduced values differed in a 32-expert
-// call.  Scalar products with packed sums were exact but no faster.
+// by add.rn.f32x2 (explicit rounding on both), did not keep the products
+// separately rounded inside the combine kernels with this toolchain: on
+// GB300 the reduced values of a 32-expert call (T = 700, H = 1024) equal
+// those of a fused multiply-add in every one of 716,800 elements and differ
+// from the separately rounded sums in 48, built with or without
+// -fmad=false (an isolated kernel doing the same pair kept them separate).
+// It was no faster either (the staged combine at 88.3 % of the copy
+// bandwidth both ways), nor were scalar products with packed sums.
 __device__ __forceinline__ void gate_add8(float* acc, float g, uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -318,13 +322,13 @@ __device__ __forceinline__ float max_partials(const float* wm, int nw, int lane)
 // PB is the partials' element size: 2 (bf16) or 4 (fp32, two 16-byte loads
 // per 8 elements); residual, weight and outputs are bf16 either way.  At
 // most 512 threads per CTA (128 registers per thread); the one-vector bf16
-// instantiations are built for two CTAs of 512 threads per SM (64
-// registers), so that the next call's CTAs can start on an SM while this
-// call's CTA still runs there.  ONE_ROW (latency-bound calls, one CTA or
+// one-row and single-CTA instantiations are built for two CTAs of 512
+// threads per SM (64 registers), so that the next call's CTAs can start on
+// an SM while this call's CTA still runs there.  ONE_ROW (latency-bound calls, one CTA or
 // cluster per row, grid = T * CS): no loop over rows, which leaves the
 // registers to fetch the weight together with the partials.
 template <int VPT, int CS, int PB = 2, bool ONE_ROW = false>
-__global__ void __launch_bounds__(512, (VPT == 1 && PB == 2) ? 2 : 1)
+__global__ void __launch_bounds__(512, (VPT == 1 && PB == 2 && (ONE_ROW || CS == 1)) ? 2 : 1)
 farn_vec_kernel(const __grid_constant__ Params p) {
   constexpr int PV = PB / 2;
   constexpr int G = (8 / (VPT * PV)) > 0 ? (8 / (VPT * PV)) : 1;
@@ -342,8 +346,8 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   __shared__ float cluster_mx[2][CS];
 
   const uint4* __restrict__ wv4 = reinterpret_cast<const uint4*>(p.weight) + (int64_t)slice * sv;
-  // One-row calls and two vectors per thread: the weight is fetched up
-  // front, alongside the partials (latency-bound calls).  Otherwise it is
+  // One-row calls and two vectors per thread: the weight is fetched with
+  // the first batch of partials (latency-bound calls).  Otherwise it is
   // fetched after the rank loop, where it holds no registers during the
   // loads and its latency hides behind the row reduction (the looping
   // one-vector build then fits 64 registers with no spill).
@@ -387,13 +391,6 @@ farn_vec_kernel(const __grid_constant__ Params p) {
   // triggering before the wait instead lets launches run many calls ahead
   // and was slower (T = 64: 3.26 us).
   if (p.prefetch) pdl_trigger();
-  if (kEarlyWeight) {
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int j = tid + k * blockDim.x;
-      if (j < sv) wv[k] = ld_keep(wv4 + j);
-    }
-  }
 
   const int64_t rows_per_pass = gridDim.x / CS;
   int it = 0;
@@ -404,26 +401,24 @@ farn_vec_kernel(const __grid_constant__ Params p) {
     uint4 rv[VPT];
     float acc[VPT][8];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int j = tid + k * blockDim.x;
-      if (j < sv) rv[k] = ld_coherent(reinterpret_cast<const uint4*>(p.residual) + base + j);
+    for (int k = 0; k < VPT; ++k)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[k][e] = -0.0f;
-    }
 
     // a1: rank sum in fp32, rank order 0..W-1, G ranks per batch of loads.
     // The first batch names its partials by constant rank indices (x[g]
-    // straight from the parameter bank); later batches index the pointer
-    // array at run time.  Measured on GB300 (W = 8, H = 4096, T = 64,
-    // back-to-back calls): 2.86 us with every batch indexed at run time,
-    // 2.40 us with the first batch constant.
-    auto batch = [&](auto first, int r0_run) {
-      const int r0 = decltype(first)::value ? 0 : r0_run;
-      uint4 xv[G][VPT][PV];
+    // straight from the parameter bank) and is issued before the residual
+    // and weight loads, which come before its adds; later batches index the
+    // pointer array at run time.  Measured on GB300 (W = 8, H = 4096,
+    // back-to-back calls, T = 64): 2.86 us with every batch indexed at run
+    // time, 2.45 us with the first batch constant and the residual loaded
+    // first, 2.34 us in this order.
+    auto load_batch = [&](int r0, bool constant_index, uint4 (&xv)[G][VPT][PV]) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const int r = r0 + g;
-        const uint4* xp = reinterpret_cast<const uint4*>(p.x[r < p.W ? r : 0]) + base * PV;
+        const uint4* xp = reinterpret_cast<const uint4*>(
+                              constant_index ? p.x[g] : p.x[r < p.W ? r : 0]) + base * PV;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           const int j = tid + k * blockDim.x;
@@ -434,6 +429,8 @@ farn_vec_kernel(const __grid_constant__ Params p) {
           }
         }
       }
+    };
+    auto add_batch = [&](int r0, const uint4 (&xv)[G][VPT][PV]) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if (r0 + g < p.W) {
@@ -445,8 +442,24 @@ farn_vec_kernel(const __grid_constant__ Params p) {
         }
       }
     };
-    batch(std::true_type(), 0);
-    for (int r0 = G; r0 < p.W; r0 += G) batch(std::false_type(), r0);
+    {
+      uint4 xv[G][VPT][PV];
+      load_batch(0, true, xv);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int j = tid + k * blockDim.x;
+        if (j < sv) {
+          rv[k] = ld_coherent(reinterpret_cast<const uint4*>(p.residual) + base + j);
+          if (kEarlyWeight) wv[k] = ld_keep(wv4 + j);
+        }
+      }
+      add_batch(0, xv);
+    }
+    for (int r0 = G; r0 < p.W; r0 += G) {
+      uint4 xv[G][VPT][PV];
+      load_batch(r0, false, xv);
+      add_batch(r0, xv);
+    }
 
     // a2 + a5: reduced and residual_out, rounded and stored; a3: the
     // thread's part of the sum of squares of the rounded residual_out.
