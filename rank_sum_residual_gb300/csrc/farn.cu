@@ -332,12 +332,13 @@ bool long_call(const farn_ctx* ctx, int64_t T, int64_t in_bytes) {
 // bf16 partials only (fp32 partials take the row kernel, see the kernel).
 bool make_stage_plan(const farn_ctx* ctx, int64_t T, int64_t H, Plan* pl, int kind) {
   const int64_t hv = H / 8;
-  // The quantising kernels try 2 vectors per thread first: at H = 8192 two
-  // CTAs of 512 threads (6 chunks in flight) measured 101.0 % (NVFP4) and
-  // 95.1 % (FP8) of the copy bandwidth against 96.4 % and 94.8 % for two
-  // CTAs of 256 threads at 4 vectors.  (The staged MoE combine measured
-  // the other way: 86.1 % at 2 vectors x 448 threads, 89.1 % at 4 x 224.)
-  const bool two_first = kind == 1 || kind == 3;
+  // The quantising kernels and the staged MoE combine try 2 vectors per
+  // thread first: at H = 8192 two CTAs of 512 threads (6 chunks in flight)
+  // measured 101.0 % (NVFP4) and 95.1 % (FP8) of the copy bandwidth against
+  // 96.4 % and 94.8 % for two CTAs of 256 threads at 4 vectors; the combine
+  // at H = 7168, K = 8, 89.7 % with two CTAs of 448 threads against 88.3 %
+  // with two of 224 at 4 vectors.
+  const bool two_first = kind == 1 || kind == 2 || kind == 3;
   const int vpts[2] = {two_first ? 2 : 4, two_first ? 4 : 2};
   if (ctx->stage_ctas > 0)   // a forced CTA count: the first vector count that fits it
     return stage_fit(ctx, hv, vpts[0], ctx->stage_ctas, pl, T, kind) ||

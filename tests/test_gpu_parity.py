@@ -930,6 +930,7 @@ def test_moe_combine_full_size_sampled(O, dev):
 @pytest.mark.parametrize("env", [dict(FARN_VARIANT="generic"), dict(FARN_VPT=1),
                                  dict(FARN_VPT=2), dict(FARN_VPT=4), dict(FARN_VARIANT="stage"),
                                  dict(FARN_VARIANT="stage", FARN_VPT=2),
+                                 dict(FARN_VARIANT="stage", FARN_VPT=4),
                                  dict(FARN_VARIANT="stage", FARN_STAGE_CTAS=1),
                                  dict(FARN_VARIANT="bulk"), dict(FARN_VARIANT="bulk", FARN_BULK_CTAS=1),
                                  dict(FARN_VARIANT="bulk", FARN_BULK_CTAS=2)],
@@ -961,10 +962,14 @@ def test_moe_combine_skipped_and_bad_slots(O, dev, variant):
         ctx.close()
 
 
-@pytest.mark.parametrize("variant", ["auto", "stage", "bulk"])
+@pytest.mark.parametrize("variant", ["auto", "stage", "stage-vpt4", "bulk"])
 def test_moe_combine_mid_size(O, dev, variant):
-    """Many rows per persistent CTA for the staged gather kernel."""
-    ctx = make_ctx(FARN_VARIANT=variant)
+    """Many rows per persistent CTA for the staged gather kernel (its
+    two-vector build, which reads the weight per row, and its four-vector
+    build, which holds it in registers)."""
+    env = dict(FARN_VARIANT="stage", FARN_VPT=4) if variant == "stage-vpt4" else \
+        dict(FARN_VARIANT=variant)
+    ctx = make_ctx(**env)
     try:
         _run_moe(O, dev, _moe(2100, 8, 7168, seed=14), ctx=ctx, what=f"moe {variant}")
     finally:
@@ -985,6 +990,8 @@ def test_moe_combine_plan(dev):
                                             w.data_ptr(), *[o.data_ptr() for o in outs])
         assert v == want, (T, v)
         assert 32 <= thr <= 512
+        if want == "stage":
+            assert thr == 448, (T, thr)      # two vectors per thread first
         if T == 4096:
             v, _ = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr() + 2,
                                               res.data_ptr(), w.data_ptr(),
