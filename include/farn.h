@@ -282,10 +282,11 @@ int farn_moe_combine(const farn_ctx *ctx,
 /* Which kernel farn_moe_combine would launch for this shape and these
  * pointers, without launching: 2 generic (any H or alignment), 3 bulk
  * (persistent CTAs that gather the rows into shared memory with TMA bulk
- * copies; chosen with FARN_BULK=1 or FARN_VARIANT=bulk at farn_create),
- * 4 stage (persistent CTAs that gather the rows into shared memory with
- * cp.async; long inputs), 5 combine (one CTA per row).  *threads receives
- * the threads per CTA.  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
+ * copies; long inputs whose rows fit two segments of at most 512 consumer
+ * threads, H <= 8192), 4 stage (persistent CTAs that gather the rows into
+ * shared memory with cp.async; other long inputs), 5 combine (one CTA per
+ * row).  *threads receives the threads per CTA (at most 544 for bulk: one
+ * producer warp and the consumers; at most 512 otherwise).  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
  * NULL pointer; aliasing is not checked). */
 int farn_plan_moe_combine(const farn_ctx *ctx, int K, int64_t T, int64_t H,
                           const void *expert_out, const void *residual,

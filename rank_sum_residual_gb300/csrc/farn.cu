@@ -147,11 +147,14 @@ struct Plan {
 // stage holds one segment of all W+1 inputs.  Chosen: the fewest segments
 // per row (fewest waits) whose ring holds at least 4 stages, else the
 // deepest ring of at least 2 stages; `ctas` resident CTAs per SM share the
-// SM's shared memory.  Rows longer than kBulkMaxH elements are not taken
+// SM's shared memory.  combine (the MoE combine, whose consumers set the
+// pace): rows of one or two segments may take up to 512 consumer threads,
+// and the fewest segments whose ring holds 2 stages win.  Rows longer than kBulkMaxH elements are not taken
 // (every shorter row is, for any W <= 32, at one CTA per SM: the longest
 // row at W = 32 takes 16 segments of 128 vectors and 3 stages).
 // force_vpt (FARN_VPT), when set, caps the segments per row.
-bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* pl) {
+bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* pl,
+              bool combine) {
   if (H > farn::kBulkMaxH) return false;
   const int64_t hv = H / 8;
   const int max_seg = ctx->force_vpt > 0 ? ctx->force_vpt : 16;
@@ -163,12 +166,16 @@ bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* 
   uint32_t best_stride = 0;
   for (int nseg = 1; nseg <= max_seg; ++nseg) {
     const int64_t nct = ((hv + nseg - 1) / nseg + 31) / 32 * 32;
-    if (nct > farn::kBulkMaxConsumers) continue;
+    if (nct > ((combine && nseg <= 2) ? farn::kBulkMaxConsumersWide : farn::kBulkMaxConsumers))
+      continue;
     if ((hv + nct - 1) / nct != nseg) continue;   // the same split as fewer segments
     const uint32_t stride = (uint32_t)((nct * 16 + 127) / 128 * 128);
     size_t ns = (budget - fixed) / ((size_t)(W + 1) * stride);
     if (ns > farn::kBulkMaxStages) ns = farn::kBulkMaxStages;
-    if (ns >= 4) { best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride; break; }
+    if (ns >= (combine ? 2u : 4u)) {
+      best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride;
+      break;
+    }
     if (ns >= 2 && ns > best_ns) { best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride; }
   }
   if (!best_seg) return false;
@@ -196,9 +203,10 @@ bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* 
 // GB300 (W = 4, T = 32768, H = 5120: 96.9 % of the copy bandwidth against
 // 89.5 % for two; W = 8, T = 8192, H = 8192: 97.0 % against 96.4 %; W = 16,
 // T = 4096, H = 7168: 98.7 % against 83.4 %).
-bool make_bulk_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, Plan* pl) {
-  if (ctx->bulk_ctas == 2 && bulk_fit(ctx, W, T, H, 2, pl)) return true;
-  return bulk_fit(ctx, W, T, H, 1, pl);
+bool make_bulk_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, Plan* pl,
+                    bool combine = false) {
+  if (ctx->bulk_ctas == 2 && bulk_fit(ctx, W, T, H, 2, pl, combine)) return true;
+  return bulk_fit(ctx, W, T, H, 1, pl, combine);
 }
 
 template <int VPT, int CS, int PB>
@@ -445,13 +453,15 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
 }
 
 // The MoE combine's kernel.  Long inputs (T >= the stage threshold): the
-// staged gather kernel, which keeps R chunks of gathered rows in flight per
-// thread (GB300, T = 4096, K = 8, H = 7168: 87.9 % of the copy bandwidth
-// against 81.3 % for one CTA per row, whose 128 registers per thread leave
-// two CTAs per SM).  Otherwise one CTA per row, every thread one vector of
-// each gathered row for few rows (all loads in flight at once), 4 vectors
-// otherwise; the generic kernel for odd shapes and alignments.
-// FARN_VARIANT=stage / row / generic force one of them.
+// TMA-staged kernel where a row fits one or two segments of at most 512
+// consumer threads (H <= 8192), else the staged gather kernel, which keeps
+// R chunks of gathered rows in flight per thread (GB300, T = 4096, K = 8,
+// H = 7168: 98.7 % of the copy bandwidth for the TMA-staged kernel, 89.9 %
+// for the staged gather, 81.3 % for one CTA per row).  Otherwise one CTA
+// per row, every thread one vector of each gathered row for few rows (all
+// loads in flight at once), 4 vectors otherwise; the generic kernel for odd
+// shapes and alignments.  FARN_VARIANT=bulk / stage / row / generic force
+// one of them; FARN_STAGE=0 leaves long inputs to the row kernel.
 int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   pl.pb = 2; pl.cs = 1; pl.stages = 0; pl.stage_stride = 0; pl.smem = 0; pl.stage_r = 0;
@@ -459,16 +469,18 @@ int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok,
   const int64_t hv = H / 8;
   const int want = ctx->force_variant;
   if (want == kVariantCluster) return FARN_ERR_UNSUPPORTED;
-  if (vec_ok && (want == kVariantBulk ||
-                 (want == kVariantAuto && ctx->bulk &&
-                  long_call(ctx, T, (int64_t)(K + 1) * T * H * 2))) &&
-      make_bulk_plan(ctx, K, T, H, &pl)) {
-    *out = pl;
+  const bool long_moe = long_call(ctx, T, (int64_t)(K + 1) * T * H * 2);
+  Plan bp;
+  if (vec_ok && (want == kVariantBulk || (want == kVariantAuto && long_moe &&
+                                          (ctx->bulk || ctx->stage))) &&
+      make_bulk_plan(ctx, K, T, H, &bp, true) &&
+      (want == kVariantBulk || ctx->bulk || bp.vpt <= 2)) {
+    *out = bp;
     return FARN_OK;
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   if (vec_ok && want != kVariantGeneric && want != kVariantRow &&
-      (want == kVariantStage || (ctx->stage && long_call(ctx, T, (int64_t)(K + 1) * T * H * 2))) &&
+      (want == kVariantStage || (ctx->stage && long_moe)) &&
       make_stage_plan(ctx, T, H, &pl, 2)) {
     *out = pl;
     return FARN_OK;

@@ -943,6 +943,19 @@ def test_moe_combine_variants(O, dev, env):
         ctx.close()
 
 
+@pytest.mark.parametrize("T,K,H", [(40, 8, 4096), (37, 8, 7168), (19, 8, 8192), (23, 8, 12288),
+                                   (9, 16, 7168), (5, 32, 16384), (11, 1, 2048)])
+def test_moe_combine_bulk_segments(O, dev, T, K, H):
+    """The TMA-staged combine over one segment of up to 512 consumer threads
+    (H <= 4096), two of up to 512 (H = 7168, 8192), and more of at most 256
+    (longer rows, or rows whose K + 1 inputs leave room for fewer stages)."""
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        _run_moe(O, dev, _moe(T, K, H, seed=T + K), ctx=ctx, what=f"moe bulk T={T} K={K} H={H}")
+    finally:
+        ctx.close()
+
+
 @pytest.mark.parametrize("variant", ["row", "stage", "bulk"])
 def test_moe_combine_skipped_and_bad_slots(O, dev, variant):
     """-1 and out-of-range slots are skipped (never read); a token with no
@@ -977,21 +990,29 @@ def test_moe_combine_mid_size(O, dev, variant):
 
 
 def test_moe_combine_plan(dev):
-    """Long inputs take the staged gather kernel, shorter ones one CTA per
-    row, odd alignments the generic kernel; FARN_VARIANT forces each."""
+    """Long inputs take the TMA-staged kernel while a row fits two segments
+    of at most 512 consumer threads, else the staged gather kernel; shorter
+    ones one CTA per row, odd alignments the generic kernel; FARN_VARIANT
+    forces each."""
     c = farn._context_for(0)
-    # staged from 2048 rows, or from 1024 rows reading >= 128 MiB
-    for T, want in ((4096, "stage"), (2047, "stage"), (1100, "stage"), (1000, "combine"),
-                    (1, "combine")):
-        p = _moe(T, 8, 7168)
+    # long from 2048 rows, or from 1024 rows reading >= 128 MiB
+    for T, H, want in ((4096, 7168, "bulk"), (2047, 7168, "bulk"), (1100, 7168, "bulk"),
+                       (1000, 7168, "combine"), (1, 7168, "combine"), (2048, 4096, "bulk"),
+                       (2048, 12288, "stage")):
+        p = _moe(T, 8, H)
         (ex, index, gates), res, w = synth.device_inputs(p, dev)
         outs = [torch.empty_like(res) for _ in range(3)]
         v, thr = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr(), res.data_ptr(),
                                             w.data_ptr(), *[o.data_ptr() for o in outs])
-        assert v == want, (T, v)
-        assert 32 <= thr <= 512
+        assert v == want, (T, H, v)
+        assert 32 <= thr <= 544
+        if want == "bulk":
+            # one producer warp and 896 / 2 (H = 7168) or 512 (H = 4096) consumers
+            assert thr == (32 + 448 if H == 7168 else 32 + 512), (T, H, thr)
         if want == "stage":
-            assert thr == 448, (T, thr)      # two vectors per thread first
+            # two vectors per thread where that fits 512 threads, else four
+            nt2 = 32 * ((H // 16 + 31) // 32)
+            assert thr == (nt2 if nt2 <= 512 else 32 * ((H // 32 + 31) // 32)), (T, H, thr)
         if T == 4096:
             v, _ = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr() + 2,
                                               res.data_ptr(), w.data_ptr(),
@@ -999,6 +1020,7 @@ def test_moe_combine_plan(dev):
             assert v == "generic"
             for env, want_v in ((dict(FARN_VARIANT="row"), "combine"),
                                 (dict(FARN_VARIANT="generic"), "generic"),
+                                (dict(FARN_VARIANT="stage"), "stage"),
                                 (dict(FARN_STAGE=0), "combine"),
                                 (dict(FARN_VARIANT="bulk"), "bulk"),
                                 (dict(FARN_BULK=1), "bulk")):
