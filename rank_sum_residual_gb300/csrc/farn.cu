@@ -147,9 +147,14 @@ struct Plan {
 // stage holds one segment of all W+1 inputs.  Chosen: the fewest segments
 // per row (fewest waits) whose ring holds at least 4 stages, else the
 // deepest ring of at least 2 stages; `ctas` resident CTAs per SM share the
-// SM's shared memory.  combine (the MoE combine, whose consumers set the
-// pace): rows of one or two segments may take up to 512 consumer threads,
-// and the fewest segments whose ring holds 2 stages win.  Rows longer than kBulkMaxH elements are not taken
+// SM's shared memory.  Where the consumers set the pace -- the MoE combine
+// (combine) and rank sums of W >= 8 inputs -- rows of one or two segments
+// may take up to 512 consumer threads, and the fewest segments whose ring
+// holds 2 stages win.  Measured on GB300 (T = 8192, H = 4096..8192): at
+// W = 8, 95.2-100.3 % of the copy bandwidth with one or two segments of up
+// to 512 consumers against 92.3-94.9 % with at most 256 and 4 stages; at
+// W = 16, 98.8-104.6 % against 97.2-102.3 %; at W = 4 the other way
+// (81.4-89.0 % against 86.2-96.0 %).  Rows longer than kBulkMaxH elements are not taken
 // (every shorter row is, for any W <= 32, at one CTA per SM: the longest
 // row at W = 32 takes 16 segments of 128 vectors and 3 stages).
 // force_vpt (FARN_VPT), when set, caps the segments per row.
@@ -161,18 +166,19 @@ bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* 
   const size_t budget = (size_t)ctx->max_smem / (size_t)ctas;
   const size_t fixed = sizeof(farn::BulkBarriers) + 128;
   if (budget <= fixed) return false;
+  const bool wide = combine || W >= 8;
   int best_seg = 0, best_nct = 0;
   size_t best_ns = 0;
   uint32_t best_stride = 0;
   for (int nseg = 1; nseg <= max_seg; ++nseg) {
     const int64_t nct = ((hv + nseg - 1) / nseg + 31) / 32 * 32;
-    if (nct > ((combine && nseg <= 2) ? farn::kBulkMaxConsumersWide : farn::kBulkMaxConsumers))
+    if (nct > ((wide && nseg <= 2) ? farn::kBulkMaxConsumersWide : farn::kBulkMaxConsumers))
       continue;
     if ((hv + nct - 1) / nct != nseg) continue;   // the same split as fewer segments
     const uint32_t stride = (uint32_t)((nct * 16 + 127) / 128 * 128);
     size_t ns = (budget - fixed) / ((size_t)(W + 1) * stride);
     if (ns > farn::kBulkMaxStages) ns = farn::kBulkMaxStages;
-    if (ns >= (combine ? 2u : 4u)) {
+    if (ns >= (wide ? 2u : 4u)) {
       best_seg = nseg; best_nct = (int)nct; best_ns = ns; best_stride = stride;
       break;
     }

@@ -884,11 +884,11 @@ farn_combine_kernel(const __grid_constant__ Params p) {
 constexpr uint32_t kBulkMaxStages = 16;
 constexpr int kBulkMaxConsumers = 256;   // consumer threads per CTA
 constexpr int kBulkThreads = 32 + kBulkMaxConsumers;
-// The MoE combine's one- and two-segment builds take up to 512 consumer
-// threads: its consumers, three rounded operations per gathered element,
-// set its pace (GB300, K = 8, H = 7168, T = 4096: 98.7 % of the copy
-// bandwidth with 448 consumer threads and 2 segments, 82.7 % with 320 and
-// 3, 79.1 % with 224 and 4).
+// The one- and two-segment builds take up to 512 consumer threads, used
+// where the consumers set the pace: the MoE combine (three rounded
+// operations per gathered element; GB300, K = 8, H = 7168, T = 4096: 98.7 %
+// of the copy bandwidth with 448 consumer threads and 2 segments, 82.7 %
+// with 320 and 3, 79.1 % with 224 and 4) and rank sums of W >= 8 inputs.
 constexpr int kBulkMaxConsumersWide = 512;
 constexpr int64_t kBulkMaxH = 16384;     // longest row the bulk plan takes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
@@ -964,8 +964,8 @@ struct BulkBarriers {
 // VPT: the most segments per row (vectors per consumer thread) this
 // instantiation takes.  The host guarantees H % 8 == 0, 16-byte aligned
 // tensors, ceil(hv / nct) <= VPT, a stage_stride of at least nct * 16 bytes
-// (a multiple of 128) and blockDim.x = 32 + nct with nct <= 256 (<= 512 for
-// the MoE combine at VPT <= 2).
+// (a multiple of 128) and blockDim.x = 32 + nct with nct <= 256 (<= 512 at
+// VPT <= 2).
 // COMBINE: the MoE combine instead of the rank sum -- the W = K inputs of
 // a row are the gathered expert rows expert_out[index[t,k]], summed as
 // gates[t,k] * x with each product and sum rounded (slots outside
@@ -973,8 +973,7 @@ struct BulkBarriers {
 // and every consumer warp's lane k hold column k of the row's routing,
 // loaded one of the CTA's rows ahead.
 template <int VPT, bool COMBINE = false>
-__global__ void __launch_bounds__((COMBINE && VPT <= 2) ? 32 + kBulkMaxConsumersWide : kBulkThreads,
-                                  1)
+__global__ void __launch_bounds__(VPT <= 2 ? 32 + kBulkMaxConsumersWide : kBulkThreads, 1)
 farn_bulk_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const uint32_t NS = p.stages;

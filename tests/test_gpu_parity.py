@@ -181,6 +181,36 @@ def test_bulk_variant(O, dev, name, T):
         ctx.close()
 
 
+@pytest.mark.parametrize("W,H,T,threads", [
+    (8, 4096, 333, 32 + 512),     # one segment of 512 consumers, 3 stages
+    (8, 8192, 419, 32 + 512),     # two segments of 512
+    (16, 5120, 257, 32 + 320),    # two segments of 320, a 2-stage ring
+    (16, 7168, 301, 32 + 224),    # two segments leave 1 stage: four of 224
+    (12, 6144, 190, 32 + 384),    # two segments of 384
+    (4, 5120, 211, 32 + 224),     # W < 8: at most 256 consumers, >= 4 stages
+    (4, 4096, 150, 32 + 256)])
+def test_bulk_consumer_split(O, dev, W, H, T, threads):
+    """The TMA-staged kernel's row split: with W >= 8 inputs a row takes one
+    or two segments of up to 512 consumer threads (the fewest segments whose
+    ring holds 2 stages), with fewer inputs at most 256 consumers and a ring
+    of at least 4 stages; every split equal to the oracle."""
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        p = synth.Problem("split", W, T, H, 1e-6, W + T, synth.N01)
+        xs, res, w = synth.device_inputs(p, dev)
+        outs = [torch.empty_like(res) for _ in range(3)]
+        plan = farn.farn_plan(ctx.handle, W, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                              w.data_ptr(), *[o.data_ptr() for o in outs])
+        assert plan[0] == "bulk" and plan[2] == threads, plan
+        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx)
+        torch.cuda.synchronize()
+        assert_parity([u16(o) for o in outs], oracle_rows(O, xs, res, w, p.eps),
+                      f"bulk split W={W} H={H}")
+        assert farn.farn_device_status(ctx.handle) == 0
+    finally:
+        ctx.close()
+
+
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_bulk_variant_ctas_per_sm(O, dev, ctas):
     """One or two resident TMA-staged CTAs per SM (FARN_BULK_CTAS)."""
