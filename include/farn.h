@@ -138,7 +138,10 @@ int farn_check_args(const void *const *partials, int W,
  * limit (2 s): 1 a consumer waiting for a staged segment, 2 the producer
  * waiting for a free stage, 4 a consumer in the row reduction, 8 the
  * producer draining its copies.  The kernel that gave up left its outputs
- * incomplete.  Returns FARN_ERR_INVALID_ARG or FARN_ERR_CUDA on failure. */
+ * incomplete.  The TMA-staged kernel runs where farn_plan /
+ * farn_plan_moe_combine report variant 3, and in every
+ * farn_forward_noalloc call.  Returns FARN_ERR_INVALID_ARG or FARN_ERR_CUDA
+ * on failure. */
 int farn_device_status(const farn_ctx *ctx, int *status);
 
 /* Release a context (NULL is accepted).  Returns FARN_OK. */
@@ -152,8 +155,9 @@ const char *farn_status_string(int status);
  * cluster of CTAs splits each row), 2 generic (any H or alignment), 3 bulk
  * (persistent CTAs whose producer warp stages column segments of every
  * input row in shared memory with TMA bulk copies; rows of at most 16384
- * elements), 4 stage (persistent CTAs whose threads stage their own
- * vectors in shared memory with cp.async).
+ * elements; long calls with W >= 12 bf16 partials, or any call when
+ * enabled), 4 stage (persistent CTAs whose threads stage their own
+ * vectors in shared memory with cp.async; other long calls).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */
 int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,

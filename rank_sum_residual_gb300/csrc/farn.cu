@@ -282,6 +282,9 @@ int env_int(const char* name, int dflt) {
 // for one CTA per row).
 // Below this many rows a latency-bound call splits rows over a cluster.
 constexpr int64_t kClusterRowsMax = 16;
+// Long calls with at least this many bf16 inputs default to the TMA-staged
+// kernel (see make_plan).
+constexpr int kBulkDefaultMinW = 12;
 
 int choose_vpt(int64_t sv) {
   if (sv >= 512) return 4;
@@ -382,8 +385,16 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   const int want = ctx->force_variant;
   const bool small = T < ctx->small_t;
   pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
+  // Long calls with many inputs take the TMA-staged kernel, the rest the
+  // cp.async-staged one.  Measured on GB300 (T = 8192, H = 2048..8192, % of
+  // the copy bandwidth, staged against TMA-staged): W = 12..32, 86.3-101.8
+  // against 91.8-105.2 %, ahead on 23 of 25 shapes (behind by at most
+  // 1.8 points); W = 8, ahead on 3 of 5 (behind by 5.3 points at H = 8192);
+  // W = 4 and 6, behind on 6 of 10.
   if (vec_ok && pb == 2 && !quant && (want == kVariantBulk ||
-                 (want == kVariantAuto && ctx->bulk && !small && ctx->force_cluster == 0)) &&
+                 (want == kVariantAuto && ctx->force_cluster == 0 &&
+                  ((ctx->bulk && !small) ||
+                   (ctx->stage && W >= kBulkDefaultMinW && long_call(ctx, T, in_bytes))))) &&
       make_bulk_plan(ctx, W, T, H, &pl)) {
     *out = pl;
     return FARN_OK;

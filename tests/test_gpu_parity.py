@@ -300,8 +300,13 @@ def test_plan_choices(dev):
             return farn.farn_plan(c.handle, W, T, H, [a] * W, a + g, a + 2 * g,
                                   a + 3 * g, a + 4 * g, a + 5 * g)
         assert plan(8, 8192, 8192) == ("stage", 1, 512)  # 2 vectors/thread, 1 CTA/SM
-        assert plan(16, 4096, 7168) == ("stage", 1, 224)  # 4 vectors/thread, 2 CTAs/SM
         assert plan(4, 32768, 5120) == ("stage", 1, 160)
+        # W >= 12 long calls: the TMA-staged kernel (producer warp + consumers)
+        assert plan(16, 4096, 7168) == ("bulk", 1, 32 + 224)   # 4 segments of 224
+        assert plan(12, 2048, 4096) == ("bulk", 1, 32 + 512)   # 1 segment of 512
+        assert plan(32, 2048, 8192) == ("bulk", 1, 32 + 192)   # 6 segments of 192, 2 stages
+        assert plan(11, 4096, 7168)[0] == "stage"
+        assert plan(16, 1000, 7168)[0] == "row"          # not a long call
         # half the row threshold when the call reads >= 128 MiB
         assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
         assert plan(8, 1023, 8192)[0] == "row"
