@@ -285,6 +285,9 @@ constexpr int64_t kClusterRowsMax = 16;
 // Long calls with at least this many bf16 inputs default to the TMA-staged
 // kernel (see make_plan).
 constexpr int kBulkDefaultMinW = 12;
+// Long calls with fewer bf16 inputs and a bf16 norm_out take the row kernel
+// (see make_plan).
+constexpr int kStageMinW = 8;
 
 int choose_vpt(int64_t sv) {
   if (sv >= 512) return 4;
@@ -401,9 +404,18 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   pl.stage_r = 0;
+  // The cp.async-staged kernel for long calls of 8..11 partials and for the
+  // FP8 / NVFP4 outputs; with fewer partials and a bf16 norm_out the row
+  // kernel (one CTA per row, the row prefetched into L2 before the
+  // dependency wait) streams faster.  Measured on GB300, % of the copy
+  // bandwidth, stage against row: nonpow2 (W = 4, T = 32768, H = 5120)
+  // 99.4 against 103.1, rmsnorm (W = 1, T = 8192, H = 8192) 95.3 against
+  // 98.2; T = 8192, H = 4096..8192: W = 1, 2, 4 behind on all 15 shapes (by
+  // 1.6-18.2 points); W = 8 ahead on 2 of 5; prefill (W = 8) 103.8 against
+  // 101.0, its FP8 / NVFP4 outputs 101.6 / 100.3 against 96.3 / 92.3.
   if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && long_call(ctx, T, in_bytes) &&
-                  ctx->force_cluster == 0)) &&
+                  (W >= kStageMinW || quant) && ctx->force_cluster == 0)) &&
       make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
     *out = pl;
     return FARN_OK;

@@ -300,7 +300,10 @@ def test_plan_choices(dev):
             return farn.farn_plan(c.handle, W, T, H, [a] * W, a + g, a + 2 * g,
                                   a + 3 * g, a + 4 * g, a + 5 * g)
         assert plan(8, 8192, 8192) == ("stage", 1, 512)  # 2 vectors/thread, 1 CTA/SM
-        assert plan(4, 32768, 5120) == ("stage", 1, 160)
+        # fewer than 8 partials and a bf16 norm_out: one CTA per row, 4 vectors
+        assert plan(4, 32768, 5120) == ("row", 1, 160)
+        assert plan(1, 8192, 8192) == ("row", 1, 256)
+        assert plan(7, 4096, 4096) == ("row", 1, 128)
         # W >= 12 long calls: the TMA-staged kernel (producer warp + consumers)
         assert plan(16, 4096, 7168) == ("bulk", 1, 32 + 224)   # 4 segments of 224
         assert plan(12, 2048, 4096) == ("bulk", 1, 32 + 512)   # 1 segment of 512
@@ -713,6 +716,13 @@ def test_f32_partials_plan(dev):
                                     flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
         assert farn.farn_plan_typed(c.handle, farn.FARN_F32, 8, 8192, 8192, *noq,
                                     flags=farn.FARN_PLAN_FP8_OUT)[0] == "row"
+        # fewer than 8 bf16 partials: the row kernel, but the stage kernel
+        # for the quantised outputs
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 8192, *args)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 8192, *args,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 8192, *noq,
+                                    flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "stage"
     finally:
         c.close()
 
