@@ -52,6 +52,8 @@ struct farn_ctx {
   int max_smem;        // opt-in shared memory per CTA, bytes
   int* d_status;       // device status word of the bulk kernel (256 B block)
   int fault_launch;    // FARN_FAULT_INJECT=launch at create: every launch fails
+  int stall_test;      // FARN_FAULT_INJECT=stall at create: the TMA-staged kernel's
+                       // CTA 0 runs its bounded waits out (a test of the status word)
 };
 
 namespace {
@@ -626,9 +628,11 @@ int farn_check_args(const void* const* partials, int W, const void* residual,
 int farn_create(farn_ctx** out, int device) {
   if (!out || device < 0) return FARN_ERR_INVALID_ARG;
   *out = nullptr;
-  // Host-side fault injection for the tests, read here once: "create" fails
-  // this call, "launch" makes every launch of the new context fail (before
-  // anything is enqueued).  No per-call environment lookups.
+  // Fault injection for the tests, read here once: "create" fails this
+  // call, "launch" makes every launch of the new context fail (before
+  // anything is enqueued), "stall" makes CTA 0 of every TMA-staged launch
+  // of the new context wait out its time limit (2 s) and report it in the
+  // status word.  No per-call environment lookups.
   const char* inject = getenv("FARN_FAULT_INJECT");
   if (inject && strcmp(inject, "create") == 0) return FARN_ERR_CUDA;
   const bool inject_launch = inject && strcmp(inject, "launch") == 0;
@@ -642,6 +646,7 @@ int farn_create(farn_ctx** out, int device) {
   if (!c) return FARN_ERR_NOMEM;
   c->device = device;
   c->fault_launch = inject_launch ? 1 : 0;
+  c->stall_test = inject && strcmp(inject, "stall") == 0 ? 1 : 0;
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
     delete c;
     cudaGetLastError();
@@ -917,6 +922,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   prm.err = ctx->d_status;
   prm.stages = pl.stages;
   prm.stage_stride = pl.stage_stride;
+  prm.stall_test = ctx->stall_test;
   prm.prefetch = (pl.variant == kVariantRow || pl.variant == kVariantCluster) &&
                  T < ctx->small_t && ctx->pdl;
 
@@ -1051,6 +1057,7 @@ int farn_moe_combine(const farn_ctx* ctx, const void* expert_out, int64_t n_slot
   prm.err = ctx->d_status;
   prm.stages = pl.stages;
   prm.stage_stride = pl.stage_stride;
+  prm.stall_test = ctx->stall_test;
 
   DeviceGuard g(ctx->device);
   if (!g.ok) { cudaGetLastError(); return FARN_ERR_CUDA; }

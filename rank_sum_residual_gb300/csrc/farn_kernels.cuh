@@ -70,6 +70,9 @@ struct Params {
   int* err;               // device status word, bits of kBulkErr* on a timeout
   uint32_t stages;        // shared-memory ring stages
   uint32_t stage_stride;  // bytes per input slot of a stage (multiple of 128)
+  // a test of the bounded waits: CTA 0's consumers wait on a barrier that
+  // nothing completes, give up after the time limit and abort the CTA
+  int stall_test;
 };
 
 // ----------------------------------------------------------- bf16 helpers
@@ -957,6 +960,7 @@ struct BulkBarriers {
   uint64_t full[kBulkMaxStages];
   uint64_t empty[kBulkMaxStages];
   uint64_t reduce[2];          // per row parity: one arrival per consumer warp
+  uint64_t never;              // nothing arrives on it (stall_test)
   float warp_ss[2][32];
   int abort_flag;
 };
@@ -1010,6 +1014,7 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
     }
     mbar_init(reduce0, (uint32_t)ncw);
     mbar_init(reduce0 + 8, (uint32_t)ncw);
+    mbar_init((uint32_t)__cvta_generic_to_shared(&bb->never), 1);
     bb->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1097,6 +1102,16 @@ farn_bulk_kernel(const __grid_constant__ Params p) {
   }
 
   // ------------------------------------------------------------ consumers
+  if (p.stall_test && blockIdx.x == 0) {
+    // The test of the bounded waits: every consumer of CTA 0 waits on a
+    // barrier nothing completes, the first past the time limit sets the
+    // abort flag and kBulkErrFull, and all of them leave; the producer sees
+    // the flag in its wait for a free stage, then drains its copies, which
+    // all complete.  CTA 0's rows are left unwritten.
+    wait_phase((uint32_t)__cvta_generic_to_shared(&bb->never), 0u, abort_flag, p.err,
+               kBulkErrFull);
+    return;
+  }
   const int ctid = tid - 32;
   const int cw = warp - 1;
   // The weight slice stays in registers across rows (up to 8 segments);

@@ -211,6 +211,50 @@ def test_bulk_consumer_split(O, dev, W, H, T, threads):
         ctx.close()
 
 
+def test_bulk_bounded_wait_expires_and_reports(O, dev):
+    """The TMA-staged kernel's waits are bounded.  With FARN_FAULT_INJECT=stall
+    (read at create) CTA 0's consumers wait on a barrier that nothing
+    completes: they give up after the 2 s limit, the kernel returns (no GPU
+    fault, nothing hangs), and the status word says which wait gave up.
+    CTA 0's rows are left unwritten, every other row equals the oracle, the
+    status read clears it, and the context's next status is clean."""
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    T, W, H = 600, 8, 4096
+    p = synth.Problem("stall", W, T, H, 1e-6, 3, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    sentinel = 0x7FC1                                    # a NaN no output can be
+    outs = [torch.full_like(res, 0).view(torch.int16).fill_(sentinel).view(torch.bfloat16)
+            for _ in range(3)]
+    ctx = make_ctx(FARN_VARIANT="bulk", FARN_FAULT_INJECT="stall")
+    try:
+        assert farn.farn_plan(ctx.handle, W, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                              w.data_ptr(), *[o.data_ptr() for o in outs])[0] == "bulk"
+        farn.forward(xs, res, w, p.eps, out=outs, ctx=ctx)
+        torch.cuda.synchronize()
+        st = farn.farn_device_status(ctx.handle)
+        # a consumer gave up (1), or the producer's own limit came first (2)
+        assert st != 0 and st & ~3 == 0, st
+        assert farn.farn_device_status(ctx.handle) == 0   # the read cleared it
+        got = [u16(o) for o in outs]
+        cta0 = np.arange(0, T, min(T, nsm))               # rows of CTA 0 (one CTA per SM)
+        for g in got:
+            assert (g[cta0] == sentinel).all()
+        rest = np.setdiff1d(np.arange(T), cta0)
+        want = oracle_rows(O, xs, res, w, p.eps)
+        assert_parity([g[rest] for g in got], [x[rest] for x in want], "bulk stall, other CTAs")
+    finally:
+        ctx.close()
+    # the same call on a context without the injection: complete and clean
+    ctx = make_ctx(FARN_VARIANT="bulk")
+    try:
+        out = farn.forward(xs, res, w, p.eps, ctx=ctx)
+        torch.cuda.synchronize()
+        assert farn.farn_device_status(ctx.handle) == 0
+        assert_parity([u16(o) for o in out], want, "bulk after stall")
+    finally:
+        ctx.close()
+
+
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_bulk_variant_ctas_per_sm(O, dev, ctas):
     """One or two resident TMA-staged CTAs per SM (FARN_BULK_CTAS)."""
