@@ -151,13 +151,16 @@ int farn_destroy(farn_ctx *ctx);
 const char *farn_status_string(int status);
 
 /* Which kernel variant farn_forward would launch for this shape and these
- * pointers, without launching: 0 row (one CTA per row), 1 cluster (a
- * cluster of CTAs splits each row), 2 generic (any H or alignment), 3 bulk
- * (persistent CTAs whose producer warp stages column segments of every
- * input row in shared memory with TMA bulk copies; rows of at most 16384
- * elements; long calls with W >= 12 bf16 partials, or any call when
- * enabled), 4 stage (persistent CTAs whose threads stage their own
- * vectors in shared memory with cp.async; other long calls).
+ * pointers, without launching: 0 row (one CTA per row; decode sizes, and
+ * long calls with a bf16 norm_out of W < 8 bf16 partials or of 8..11 with
+ * H <= 5120), 1 cluster (a cluster of CTAs splits each row; fewer than 16
+ * rows), 2 generic (any H or alignment), 3 bulk (persistent CTAs whose
+ * producer warp stages column segments of every input row in shared memory
+ * with TMA bulk copies; rows of at most 16384 elements; long calls of
+ * W >= 12 bf16 partials or of 8..11 with 5120 < H < 8192, or any call
+ * when enabled), 4 stage (persistent CTAs whose threads stage their own
+ * vectors in shared memory with cp.async; the other long calls: 8..11
+ * partials with H >= 8192, and the FP8 / NVFP4 outputs).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */
 int farn_plan(const farn_ctx *ctx, int W, int64_t T, int64_t H,

@@ -290,6 +290,11 @@ constexpr int kBulkDefaultMinW = 12;
 // Long calls with fewer bf16 inputs and a bf16 norm_out take the row kernel
 // (see make_plan).
 constexpr int kStageMinW = 8;
+// With kStageMinW <= W < kBulkDefaultMinW the row length decides: rows of at
+// most kRowMaxH elements take the row kernel, rows shorter than kStageMinH
+// the TMA-staged kernel, longer ones the cp.async-staged kernel.
+constexpr int64_t kRowMaxH = 5120;
+constexpr int64_t kStageMinH = 8192;
 
 int choose_vpt(int64_t sv) {
   if (sv >= 512) return 4;
@@ -396,20 +401,31 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   // against 91.8-105.2 %, ahead on 23 of 25 shapes (behind by at most
   // 1.8 points); W = 8, ahead on 3 of 5 (behind by 5.3 points at H = 8192);
   // W = 4 and 6, behind on 6 of 10.
-  if (vec_ok && pb == 2 && !quant && (want == kVariantBulk ||
-                 (want == kVariantAuto && ctx->force_cluster == 0 &&
-                  ((ctx->bulk && !small) ||
-                   (ctx->stage && W >= kBulkDefaultMinW && long_call(ctx, T, in_bytes))))) &&
+  // With 8..11 partials (T = 8192, % of the copy bandwidth, W = 8 / 10, row /
+  // TMA-staged / cp.async-staged): H = 3072..5120 the row kernel leads
+  // (95.8-100.6 against 91.9-101.5 / 90.6-92.3); H = 6144 and 7168 the
+  // TMA-staged kernel (97.3-105.7 against 90.5-96.7 / 94.2-97.2); H = 8192
+  // and above the cp.async-staged kernel (96.7-106.6 against 88.4-100.9 /
+  // 96.3-104.8).
+  const bool mid_w = W >= kStageMinW && W < kBulkDefaultMinW;
+  const bool auto_long = want == kVariantAuto && ctx->force_cluster == 0 && ctx->stage &&
+                         long_call(ctx, T, in_bytes);
+  const bool bulk_default =
+      auto_long && (W >= kBulkDefaultMinW || (mid_w && H > kRowMaxH && H < kStageMinH));
+  const bool bulk_enabled = want == kVariantAuto && ctx->force_cluster == 0 && ctx->bulk && !small;
+  if (vec_ok && pb == 2 && !quant &&
+      (want == kVariantBulk || bulk_enabled || bulk_default) &&
       make_bulk_plan(ctx, W, T, H, &pl)) {
     *out = pl;
     return FARN_OK;
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   pl.stage_r = 0;
-  // The cp.async-staged kernel for long calls of 8..11 partials and for the
-  // FP8 / NVFP4 outputs; with fewer partials and a bf16 norm_out the row
-  // kernel (one CTA per row, the row prefetched into L2 before the
-  // dependency wait) streams faster.  Measured on GB300, % of the copy
+  // The cp.async-staged kernel for long calls of 8..11 partials with rows of
+  // 8192 elements or more (shorter ones over 5120 took the TMA-staged kernel
+  // above) and for the FP8 / NVFP4 outputs; with fewer partials or shorter
+  // rows and a bf16 norm_out the row kernel (one CTA per row, the row
+  // prefetched into L2 before the dependency wait) streams faster.  Measured on GB300, % of the copy
   // bandwidth, stage against row: nonpow2 (W = 4, T = 32768, H = 5120)
   // 99.4 against 103.1, rmsnorm (W = 1, T = 8192, H = 8192) 95.3 against
   // 98.2; T = 8192, H = 4096..8192: W = 1, 2, 4 behind on all 15 shapes (by
@@ -417,7 +433,7 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   // 101.0, its FP8 / NVFP4 outputs 101.6 / 100.3 against 96.3 / 92.3.
   if (vec_ok && pb == 2 && (want == kVariantStage ||
                  (want == kVariantAuto && ctx->stage && long_call(ctx, T, in_bytes) &&
-                  (W >= kStageMinW || quant) && ctx->force_cluster == 0)) &&
+                  (quant || (W >= kStageMinW && H > kRowMaxH)) && ctx->force_cluster == 0)) &&
       make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
     *out = pl;
     return FARN_OK;

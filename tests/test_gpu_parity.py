@@ -352,7 +352,12 @@ def test_plan_choices(dev):
         assert plan(16, 4096, 7168) == ("bulk", 1, 32 + 224)   # 4 segments of 224
         assert plan(12, 2048, 4096) == ("bulk", 1, 32 + 512)   # 1 segment of 512
         assert plan(32, 2048, 8192) == ("bulk", 1, 32 + 192)   # 6 segments of 192, 2 stages
-        assert plan(11, 4096, 7168)[0] == "stage"
+        # 8..11 partials: the row length decides
+        assert plan(11, 4096, 7168)[0] == "bulk"
+        assert plan(8, 4096, 6144)[0] == "bulk"
+        assert plan(8, 4096, 5120)[0] == "row"
+        assert plan(10, 4096, 4096)[0] == "row"
+        assert plan(8, 4096, 12288)[0] == "stage"
         assert plan(16, 1000, 7168)[0] == "row"          # not a long call
         # half the row threshold when the call reads >= 128 MiB
         assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
