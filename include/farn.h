@@ -76,9 +76,17 @@ typedef struct farn_ctx farn_ctx;
  * Queries the SM count and cluster limits, sets kernel attributes and
  * allocates one 256-byte device block (the status word of the TMA-staged
  * kernel, see farn_device_status).  The caller's current device is left
- * as it was.
- * Returns FARN_ERR_INVALID_ARG if out is NULL or device < 0,
- * FARN_ERR_CUDA if the device cannot be queried, FARN_ERR_NOMEM. */
+ * as it was.  The environment is read here and only here: FARN_VARIANT,
+ * FARN_CLUSTER, FARN_VPT, FARN_PDL, FARN_SMALL_T, FARN_BULK,
+ * FARN_BULK_CTAS, FARN_STAGE, FARN_STAGE_R, FARN_STAGE_CTAS,
+ * FARN_STAGE_MIN_T and FARN_STAGE_MIN_MB override the kernel choice (tests
+ * and sweeps); FARN_FAULT_INJECT injects a fault for the tests: "create"
+ * fails this call, "launch" makes every launch of the context fail before
+ * anything is enqueued, "stall" makes CTA 0 of every TMA-staged launch
+ * wait out its time limit and report it in the status word.
+ * Returns FARN_ERR_INVALID_ARG if out is NULL or device < 0 or not a device
+ * of this process, FARN_ERR_CUDA if the device cannot be queried (or
+ * FARN_FAULT_INJECT=create), FARN_ERR_NOMEM. */
 int farn_create(farn_ctx **out, int device);
 
 /* The fused operator on `stream` (asynchronous; the call does not wait
