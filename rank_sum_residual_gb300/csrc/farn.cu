@@ -249,19 +249,25 @@ VecKernel pick_vec_pb(int vpt, int cs) {
 
 // The one-row instantiations (bf16 partials, one vector per thread) that
 // serve latency-bound calls.
-VecKernel pick_vec_one_row(int cs) {
+template <bool QUANT>
+VecKernel pick_vec_one_row_q(int cs) {
   switch (cs) {
-    case 1: return &farn::farn_vec_kernel<1, 1, 2, true>;
-    case 2: return &farn::farn_vec_kernel<1, 2, 2, true>;
-    case 4: return &farn::farn_vec_kernel<1, 4, 2, true>;
-    case 8: return &farn::farn_vec_kernel<1, 8, 2, true>;
-    case 16: return &farn::farn_vec_kernel<1, 16, 2, true>;
+    case 1: return &farn::farn_vec_kernel<1, 1, 2, true, QUANT>;
+    case 2: return &farn::farn_vec_kernel<1, 2, 2, true, QUANT>;
+    case 4: return &farn::farn_vec_kernel<1, 4, 2, true, QUANT>;
+    case 8: return &farn::farn_vec_kernel<1, 8, 2, true, QUANT>;
+    case 16: return &farn::farn_vec_kernel<1, 16, 2, true, QUANT>;
   }
   return nullptr;
 }
 
-VecKernel pick_vec(int vpt, int cs, int pb, bool one_row = false) {
-  if (one_row) return vpt == 1 && pb == 2 ? pick_vec_one_row(cs) : nullptr;
+// quant: the call writes an FP8 or NVFP4 output (only the one-row builds
+// come in two versions; the others always carry that code)
+VecKernel pick_vec(int vpt, int cs, int pb, bool one_row = false, bool quant = true) {
+  if (one_row) {
+    if (vpt != 1 || pb != 2) return nullptr;
+    return quant ? pick_vec_one_row_q<true>(cs) : pick_vec_one_row_q<false>(cs);
+  }
   return pb == 4 ? pick_vec_pb<4>(vpt, cs) : pick_vec_pb<2>(vpt, cs);
 }
 
@@ -676,11 +682,12 @@ int farn_create(farn_ctx** out, int device) {
     if (cudaFuncSetAttribute((const void*)k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       bool ok16 = true;
-      for (int i = 0; i < 7 && ok16; ++i) {
+      for (int i = 0; i < 8 && ok16; ++i) {
         // the looping kernels (three vector counts, bf16 and fp32
-        // partials) and the one-row kernel
+        // partials) and the one-row kernels (with and without the
+        // quantised outputs)
         const int vpt = i < 6 ? 1 << (i % 3) : 1, pb = (i >= 3 && i < 6) ? 4 : 2;
-        VecKernel k = pick_vec(vpt, 16, pb, i == 6);
+        VecKernel k = pick_vec(vpt, 16, pb, i >= 6, i == 6);
         if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
             cudaSuccess) { ok16 = false; break; }
         cudaLaunchConfig_t cfg = {};
@@ -979,7 +986,7 @@ static int forward_impl(const farn_ctx* ctx, const void* const* partials, int pa
   } else if (pl.variant == kVariantStage) {
     err = cudaLaunchKernelEx(&cfg, pick_stage(pl.vpt, pl.stage_r, qm), prm);
   } else {
-    VecKernel k = pick_vec(pl.vpt, pl.cs, pb, pl.one_row);
+    VecKernel k = pick_vec(pl.vpt, pl.cs, pb, pl.one_row, qm != kQuantNone);
     err = cudaLaunchKernelEx(&cfg, k, prm);
   }
   if (err != cudaSuccess) {

@@ -329,8 +329,12 @@ __device__ __forceinline__ float max_partials(const float* wm, int nw, int lane)
 // threads per SM (64 registers), so that the next call's CTAs can start on
 // an SM while this call's CTA still runs there.  ONE_ROW (latency-bound calls, one CTA or
 // cluster per row, grid = T * CS): no loop over rows, which leaves the
-// registers to fetch the weight together with the partials.
-template <int VPT, int CS, int PB = 2, bool ONE_ROW = false>
+// registers to fetch the weight together with the partials.  QUANT: the
+// FP8 / NVFP4 outputs are compiled in; the one-row builds of plain calls
+// leave them out, which shortens their code (GB300, W = 8, H = 4096,
+// back-to-back calls: T = 1 / 8 / 64 at 1.98 / 2.14 / 2.41 us against
+// 2.03 / 2.19 / 2.44 us with them in).
+template <int VPT, int CS, int PB = 2, bool ONE_ROW = false, bool QUANT = true>
 __global__ void __launch_bounds__(512, (VPT == 1 && PB == 2 && (ONE_ROW || CS == 1)) ? 2 : 1)
 farn_vec_kernel(const __grid_constant__ Params p) {
   constexpr int PV = PB / 2;
@@ -568,7 +572,7 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       }
     }
 
-    if (p.q_out) {
+    if (QUANT && p.q_out) {
       // FP8 output: the row's amax of the bf16 norm_out (fmaxf ignores NaN;
       // max is exact, so every CTA and thread gets the same value), then
       // E4M3(norm_out * (448 / amax)) for each element.
@@ -610,7 +614,7 @@ farn_vec_kernel(const __grid_constant__ Params p) {
       if (tid == 0 && slice == 0) p.scale_out[row] = scale;
     }
 
-    if (p.fp4_q) {
+    if (QUANT && p.fp4_q) {
       // NVFP4 output: blocks of 16 elements are vector pairs (j, j ^ 1) of
       // neighbouring lanes (the host keeps the slice's vector count even).
 #pragma unroll
