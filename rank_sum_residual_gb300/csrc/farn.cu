@@ -437,9 +437,14 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   // 98.2; T = 8192, H = 4096..8192: W = 1, 2, 4 behind on all 15 shapes (by
   // 1.6-18.2 points); W = 8 ahead on 2 of 5; prefill (W = 8) 103.8 against
   // 101.0, its FP8 / NVFP4 outputs 101.6 / 100.3 against 96.3 / 92.3.
-  if (vec_ok && pb == 2 && (want == kVariantStage ||
-                 (want == kVariantAuto && ctx->stage && long_call(ctx, T, in_bytes) &&
-                  (quant || (W >= kStageMinW && H > kRowMaxH)) && ctx->force_cluster == 0)) &&
+  // With the FP8 / NVFP4 outputs (T = 8192, % of the copy bandwidth, stage
+  // against row): W = 1, the row kernel ahead at every H = 4096..8192 (by
+  // 1.9-18.0 points); W = 4, ahead at H <= 5120 (by 3.4-11.4), level at
+  // 7168, behind at 8192; W = 8, behind at H >= 5120.
+  const bool stage_default =
+      auto_long && (quant ? !(W == 1 || (W < kStageMinW && H <= kRowMaxH))
+                          : (W >= kStageMinW && H > kRowMaxH));
+  if (vec_ok && pb == 2 && (want == kVariantStage || stage_default) &&
       make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
     *out = pl;
     return FARN_OK;

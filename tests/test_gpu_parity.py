@@ -376,6 +376,30 @@ def test_plan_choices(dev):
         c.close()
 
 
+@pytest.mark.parametrize("W,H,T,want", [(10, 4096, 2100, "row"), (9, 6144, 2050, "bulk"),
+                                         (11, 8192, 2049, "stage"), (12, 3072, 2111, "bulk"),
+                                         (5, 7168, 2222, "row")])
+def test_long_call_default_plans(O, dev, W, H, T, want):
+    """Long calls through the default plan, one per kernel the row length
+    and the partial count pick (row / TMA-staged / cp.async-staged), a
+    ragged row count each, sampled rows against the oracle."""
+    c = farn._context_for(0)
+    p = synth.Problem("long", W, T, H, 1e-6, W * T, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    outs = [torch.empty_like(res) for _ in range(3)]
+    plan = farn.farn_plan(c.handle, W, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                          w.data_ptr(), *[o.data_ptr() for o in outs])
+    assert plan[0] == want, plan
+    farn.forward(xs, res, w, p.eps, out=outs)
+    torch.cuda.synchronize()
+    rows = sample_rows(T, 64, seed=W)
+    idx = torch.as_tensor(rows, device=dev)
+    got = [u16(o.index_select(0, idx)) for o in outs]
+    assert_parity(got, oracle_rows(O, xs, res, w, p.eps, rows=rows), f"default plan W={W} H={H}")
+    del xs, res, w, outs
+    torch.cuda.empty_cache()
+
+
 def test_deterministic(dev):
     p = synth.workload("decode")[-1]
     a = _variant_outputs(dev, p, None)[3]
@@ -772,6 +796,13 @@ def test_f32_partials_plan(dev):
                                     flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 8192, *noq,
                                     flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "stage"
+        # quantised outputs of one partial, or of short rows: the row kernel
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 1, 8192, 8192, *noq,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 4096, *noq,
+                                    flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 4096, *noq,
+                                    flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
     finally:
         c.close()
 
