@@ -299,10 +299,11 @@ int farn_moe_combine(const farn_ctx *ctx,
 /* Which kernel farn_moe_combine would launch for this shape and these
  * pointers, without launching: 2 generic (any H or alignment), 3 bulk
  * (persistent CTAs that gather the rows into shared memory with TMA bulk
- * copies; long inputs whose rows fit two segments of at most 512 consumer
- * threads, H <= 8192), 4 stage (persistent CTAs that gather the rows into
- * shared memory with cp.async; other long inputs), 5 combine (one CTA per
- * row).  *threads receives the threads per CTA (at most 544 for bulk: one
+ * copies; long inputs with rows of more than 3072 elements, or 5120 below
+ * 8 experts, that fit two segments of at most 512 consumer threads or more
+ * segments of 256), 4 stage (persistent CTAs that gather the rows into
+ * shared memory with cp.async; the other long inputs with such rows),
+ * 5 combine (one CTA per row; shorter inputs and shorter rows).  *threads receives the threads per CTA (at most 544 for bulk: one
  * producer warp and the consumers; at most 512 otherwise).  Returns a farn_status (FARN_ERR_INVALID_ARG for a bad shape or a
  * NULL pointer; aliasing is not checked). */
 int farn_plan_moe_combine(const farn_ctx *ctx, int K, int64_t T, int64_t H,

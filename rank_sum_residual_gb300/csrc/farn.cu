@@ -510,15 +510,16 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   return FARN_OK;
 }
 
-// The MoE combine's kernel.  Long inputs (T >= the stage threshold): the
-// TMA-staged kernel where a row fits one or two segments of at most 512
-// consumer threads (H <= 8192), else the staged gather kernel, which keeps
-// R chunks of gathered rows in flight per thread (GB300, T = 4096, K = 8,
-// H = 7168: 98.7 % of the copy bandwidth for the TMA-staged kernel, 89.9 %
-// for the staged gather, 81.3 % for one CTA per row).  Otherwise one CTA
-// per row, every thread one vector of each gathered row for few rows (all
-// loads in flight at once), 4 vectors otherwise; the generic kernel for odd
-// shapes and alignments.  FARN_VARIANT=bulk / stage / row / generic force
+// The MoE combine's kernel.  Long inputs (T >= the stage threshold) with
+// rows longer than 3072 elements (5120 below 8 experts): the TMA-staged
+// kernel where a row fits one or two segments of at most 512 consumer
+// threads, or more segments of the full 256, else the staged gather kernel,
+// which keeps R chunks of gathered rows in flight per thread (GB300,
+// T = 4096, K = 8, H = 7168: 98.7 % of the copy bandwidth for the
+// TMA-staged kernel, 89.9 % for the staged gather, 81.3 % for one CTA per
+// row).  Otherwise one CTA per row, every thread one vector of each
+// gathered row for few rows (all loads in flight at once), 4 vectors
+// otherwise; the generic kernel for odd shapes and alignments.  FARN_VARIANT=bulk / stage / row / generic force
 // one of them; FARN_STAGE=0 leaves long inputs to the row kernel.
 int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
@@ -528,17 +529,28 @@ int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok,
   const int want = ctx->force_variant;
   if (want == kVariantCluster) return FARN_ERR_UNSUPPORTED;
   const bool long_moe = long_call(ctx, T, (int64_t)(K + 1) * T * H * 2);
+  // Short rows keep the one-CTA-per-row combine kernel even for long calls.
+  // Measured on GB300 (T = 4096, % of the copy bandwidth, row / TMA-staged
+  // / staged gather): H <= 3072, 69.7-86.2 against 46.1-76.4 / 54.5-64.8
+  // (K = 2..16); H = 4096 and 5120 with K <= 6, 82.1-85.3 against
+  // 72.8-84.8 / 67.1-79.7.  The TMA-staged kernel also takes rows that need
+  // more than two segments when they still get the full 256 consumers
+  // (K = 16, H = 8192: 92.0 against 77.8 for the staged gather; K = 8,
+  // H = 10240 / 12288: 85.6 / 87.9 against 77.4 / 84.2) but not with fewer
+  // (K = 16, H = 7168, 224 consumers: 83.7 against 91.9).
+  const bool moe_row = H <= 3072 || (H <= 5120 && K < 8);
   Plan bp;
-  if (vec_ok && (want == kVariantBulk || (want == kVariantAuto && long_moe &&
-                                          (ctx->bulk || ctx->stage))) &&
+  if (vec_ok && (want == kVariantBulk ||
+                 (want == kVariantAuto && long_moe && (ctx->bulk || (ctx->stage && !moe_row)))) &&
       make_bulk_plan(ctx, K, T, H, &bp, true) &&
-      (want == kVariantBulk || ctx->bulk || bp.vpt <= 2)) {
+      (want == kVariantBulk || ctx->bulk || bp.vpt <= 2 ||
+       bp.threads - 32 == farn::kBulkMaxConsumers)) {
     *out = bp;
     return FARN_OK;
   }
   if (want == kVariantBulk) return FARN_ERR_UNSUPPORTED;
   if (vec_ok && want != kVariantGeneric && want != kVariantRow &&
-      (want == kVariantStage || (ctx->stage && long_moe)) &&
+      (want == kVariantStage || (ctx->stage && long_moe && !moe_row)) &&
       make_stage_plan(ctx, T, H, &pl, 2)) {
     *out = pl;
     return FARN_OK;

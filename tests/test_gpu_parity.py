@@ -1121,19 +1121,24 @@ def test_moe_combine_plan(dev):
     forces each."""
     c = farn._context_for(0)
     # long from 2048 rows, or from 1024 rows reading >= 128 MiB
-    for T, H, want in ((4096, 7168, "bulk"), (2047, 7168, "bulk"), (1100, 7168, "bulk"),
-                       (1000, 7168, "combine"), (1, 7168, "combine"), (2048, 4096, "bulk"),
-                       (2048, 12288, "stage")):
-        p = _moe(T, 8, H)
+    for T, K, H, want in ((4096, 8, 7168, "bulk"), (2047, 8, 7168, "bulk"),
+                          (1100, 8, 7168, "bulk"), (1000, 8, 7168, "combine"),
+                          (1, 8, 7168, "combine"), (2048, 8, 4096, "bulk"),
+                          (2048, 8, 12288, "bulk"),      # 6 segments of the full 256
+                          (2048, 16, 7168, "stage"),     # 4 segments of only 224
+                          (2048, 4, 4096, "combine"),    # short rows, few experts
+                          (2048, 8, 3072, "combine")):   # short rows
+        p = _moe(T, K, H)
         (ex, index, gates), res, w = synth.device_inputs(p, dev)
         outs = [torch.empty_like(res) for _ in range(3)]
-        v, thr = farn.farn_plan_moe_combine(c.handle, 8, T, p.H, ex.data_ptr(), res.data_ptr(),
+        v, thr = farn.farn_plan_moe_combine(c.handle, K, T, p.H, ex.data_ptr(), res.data_ptr(),
                                             w.data_ptr(), *[o.data_ptr() for o in outs])
-        assert v == want, (T, H, v)
+        assert v == want, (T, K, H, v)
         assert 32 <= thr <= 544
         if want == "bulk":
-            # one producer warp and 896 / 2 (H = 7168) or 512 (H = 4096) consumers
-            assert thr == (32 + 448 if H == 7168 else 32 + 512), (T, H, thr)
+            # one producer warp and 896 / 2 (H = 7168), 512 (H = 4096) or the
+            # full 256 (H = 12288) consumers
+            assert thr == 32 + {7168: 448, 4096: 512, 12288: 256}[H], (T, H, thr)
         if want == "stage":
             # two vectors per thread where that fits 512 threads, else four
             nt2 = 32 * ((H // 16 + 31) // 32)
