@@ -161,15 +161,15 @@ const char *farn_status_string(int status);
 /* Which kernel variant farn_forward would launch for this shape and these
  * pointers, without launching: 0 row (one CTA per row; decode sizes, and
  * long calls with a bf16 norm_out of W < 8 bf16 partials or of 8..11 with
- * H <= 5120, or with an FP8 / NVFP4 output of one partial or of W < 8 with
- * H <= 5120), 1 cluster (a cluster of CTAs splits each row; fewer than 16
+ * H <= 5120, or with an FP8 / NVFP4 output of one or two partials or of
+ * W < 8 with H <= 5120), 1 cluster (a cluster of CTAs splits each row; fewer than 16
  * rows), 2 generic (any H or alignment), 3 bulk (persistent CTAs whose
  * producer warp stages column segments of every input row in shared memory
  * with TMA bulk copies; rows of at most 16384 elements; long calls of
  * W >= 12 bf16 partials or of 8..11 with 5120 < H < 8192, or any call
  * when enabled), 4 stage (persistent CTAs whose threads stage their own
  * vectors in shared memory with cp.async; the other long calls: 8..11
- * partials with H >= 8192, and the FP8 / NVFP4 outputs of W >= 2 partials
+ * partials with H >= 8192, and the FP8 / NVFP4 outputs of W >= 3 partials
  * with H > 5120 or of W >= 8).
  * *cluster_size receives the CTAs per row (1 for row and generic),
  * *threads the threads per CTA.  Returns a farn_status. */

@@ -439,10 +439,11 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   // 101.0, its FP8 / NVFP4 outputs 101.6 / 100.3 against 96.3 / 92.3.
   // With the FP8 / NVFP4 outputs (T = 8192, % of the copy bandwidth, stage
   // against row): W = 1, the row kernel ahead at every H = 4096..8192 (by
-  // 1.9-18.0 points); W = 4, ahead at H <= 5120 (by 3.4-11.4), level at
-  // 7168, behind at 8192; W = 8, behind at H >= 5120.
+  // 1.9-18.0 points); W = 2, ahead at H = 8192 (95.1 against 86.1); W = 4,
+  // ahead at H <= 5120 (by 3.4-11.4), level at 7168, behind at 8192;
+  // W = 8, behind at H >= 5120.
   const bool stage_default =
-      auto_long && (quant ? !(W == 1 || (W < kStageMinW && H <= kRowMaxH))
+      auto_long && (quant ? !(W <= 2 || (W < kStageMinW && H <= kRowMaxH))
                           : (W >= kStageMinW && H > kRowMaxH));
   if (vec_ok && pb == 2 && (want == kVariantStage || stage_default) &&
       make_stage_plan(ctx, T, H, &pl, qm == kQuantFp8 ? 1 : (qm == kQuantNvfp4 ? 3 : 0))) {
@@ -486,6 +487,11 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
     if (ctx->force_vpt > 0) vpt = ctx->force_vpt;
     else if (small) vpt = sv <= 512 ? 1 : (sv <= 1024 ? 2 : 4);   // loads in one batch
     else vpt = choose_vpt(sv);
+    // Many rows of one or two bf16 partials and 256..511 vectors: 4 vectors
+    // per thread rather than 2 (GB300, T = 8192, H = 2048: W = 1 / 2 at 93.4
+    // / 95.5 % of the copy bandwidth against 84.5 / 91.9 %, with the FP8
+    // output 81.4 / 90.2 % against 69.8 / 79.6 %; at W = 4 two stay ahead).
+    if (!small && ctx->force_vpt == 0 && pb == 2 && W <= 2 && sv >= 256 && sv < 512) vpt = 4;
     int64_t threads = (sv + vpt - 1) / vpt;
     threads = (threads + 31) / 32 * 32;
     if (threads > 512) {

@@ -796,9 +796,16 @@ def test_f32_partials_plan(dev):
                                     flags=farn.FARN_PLAN_FP8_OUT)[0] == "stage"
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 8192, *noq,
                                     flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "stage"
-        # quantised outputs of one partial, or of short rows: the row kernel
+        # quantised outputs of one or two partials, or of short rows: the row kernel
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 1, 8192, 8192, *noq,
                                     flags=farn.FARN_PLAN_FP8_OUT)[0] == "row"
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 2, 8192, 8192, *noq,
+                                    flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "row"
+        # many rows of one or two partials and 256..511 vectors: 4 per thread
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 1, 8192, 2048, *args) == \
+            ("row", 1, 64)
+        assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 2048, *args) == \
+            ("row", 1, 128)
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 4, 8192, 4096, *noq,
                                     flags=farn.FARN_PLAN_NVFP4_OUT)[0] == "row"
         assert farn.farn_plan_typed(c.handle, farn.FARN_BF16, 8, 8192, 4096, *noq,
