@@ -255,6 +255,35 @@ def test_bulk_bounded_wait_expires_and_reports(O, dev):
         ctx.close()
 
 
+def test_bulk_moe_bounded_wait_expires_and_reports(O, dev):
+    """The same bounded-wait expiry through the MoE combine's TMA-staged
+    kernel (its default for long calls): CTA 0's rows unwritten, the status
+    word set and cleared by its read, every other row equal to the oracle."""
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    p = _moe(500, 8, 4096, seed=21)
+    (ex, index, gates), res, w = synth.device_inputs(p, dev)
+    sentinel = 0x7FC1
+    outs = tuple(torch.empty_like(res).view(torch.int16).fill_(sentinel).view(torch.bfloat16)
+                 for _ in range(3))
+    ctx = make_ctx(FARN_VARIANT="bulk", FARN_FAULT_INJECT="stall")
+    try:
+        farn.moe_combine(ex, index, gates, res, w, p.eps, out=outs, ctx=ctx)
+        torch.cuda.synchronize()
+        st = farn.farn_device_status(ctx.handle)
+        assert st != 0 and st & ~3 == 0, st
+        assert farn.farn_device_status(ctx.handle) == 0
+    finally:
+        ctx.close()
+    got = [u16(o) for o in outs]
+    cta0 = np.arange(0, p.T, min(p.T, nsm))
+    for g in got:
+        assert (g[cta0] == sentinel).all()
+    rest = np.setdiff1d(np.arange(p.T), cta0)
+    want = O.moe_combine(u16(ex), index.cpu().numpy(), gates.cpu().numpy(), u16(res), u16(w),
+                         p.eps)
+    assert_parity([g[rest] for g in got], [x[rest] for x in want], "moe bulk stall, other CTAs")
+
+
 @pytest.mark.parametrize("ctas", [1, 2])
 def test_bulk_variant_ctas_per_sm(O, dev, ctas):
     """One or two resident TMA-staged CTAs per SM (FARN_BULK_CTAS)."""
@@ -396,6 +425,29 @@ def test_long_call_default_plans(O, dev, W, H, T, want):
     idx = torch.as_tensor(rows, device=dev)
     got = [u16(o.index_select(0, idx)) for o in outs]
     assert_parity(got, oracle_rows(O, xs, res, w, p.eps, rows=rows), f"default plan W={W} H={H}")
+    del xs, res, w, outs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("H,want", [(5120, "row"), (5128, "bulk"), (8184, "bulk"), (8192, "stage")])
+def test_mid_w_row_length_boundaries(O, dev, H, want):
+    """8 partials on each side of the row-length limits of the default plan
+    (5120 for the row kernel, 8192 for the staged one), ragged row count,
+    sampled rows against the oracle."""
+    c = farn._context_for(0)
+    T = 2051
+    p = synth.Problem("edge", 8, T, H, 1e-6, H, synth.N01)
+    xs, res, w = synth.device_inputs(p, dev)
+    outs = [torch.empty_like(res) for _ in range(3)]
+    plan = farn.farn_plan(c.handle, 8, T, H, [x.data_ptr() for x in xs], res.data_ptr(),
+                          w.data_ptr(), *[o.data_ptr() for o in outs])
+    assert plan[0] == want, plan
+    farn.forward(xs, res, w, p.eps, out=outs)
+    torch.cuda.synchronize()
+    rows = sample_rows(T, 48, seed=H)
+    idx = torch.as_tensor(rows, device=dev)
+    assert_parity([u16(o.index_select(0, idx)) for o in outs],
+                  oracle_rows(O, xs, res, w, p.eps, rows=rows), f"boundary H={H}")
     del xs, res, w, outs
     torch.cuda.empty_cache()
 
