@@ -156,9 +156,9 @@ struct Plan {
 // W = 8, 95.2-100.3 % of the copy bandwidth with one or two segments of up
 // to 512 consumers against 92.3-94.9 % with at most 256 and 4 stages; at
 // W = 16, 98.8-104.6 % against 97.2-102.3 %; at W = 4 the other way
-// (81.4-89.0 % against 86.2-96.0 %).  Rows longer than kBulkMaxH elements are not taken
-// (every shorter row is, for any W <= 32, at one CTA per SM: the longest
-// row at W = 32 takes 16 segments of 128 vectors and 3 stages).
+// (81.4-89.0 % against 86.2-96.0 %).  Rows longer than kBulkMaxH elements
+// are not taken (every shorter row is, for any W <= 32, at one CTA per SM:
+// the longest row at W = 32 takes 16 segments of 128 vectors and 3 stages).
 // force_vpt (FARN_VPT), when set, caps the segments per row.
 bool bulk_fit(const farn_ctx* ctx, int W, int64_t T, int64_t H, int ctas, Plan* pl,
               bool combine) {
@@ -401,8 +401,8 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   const int want = ctx->force_variant;
   const bool small = T < ctx->small_t;
   pl.stages = 0; pl.stage_stride = 0; pl.smem = 0;
-  // Long calls with many inputs take the TMA-staged kernel, the rest the
-  // cp.async-staged one.  Measured on GB300 (T = 8192, H = 2048..8192, % of
+  // Long calls of W >= 12 bf16 partials (no quantised output) take the
+  // TMA-staged kernel.  Measured on GB300 (T = 8192, H = 2048..8192, % of
   // the copy bandwidth, staged against TMA-staged): W = 12..32, 86.3-101.8
   // against 91.8-105.2 %, ahead on 23 of 25 shapes (behind by at most
   // 1.8 points); W = 8, ahead on 3 of 5 (behind by 5.3 points at H = 8192);
@@ -525,8 +525,9 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
 // TMA-staged kernel, 89.9 % for the staged gather, 81.3 % for one CTA per
 // row).  Otherwise one CTA per row, every thread one vector of each
 // gathered row for few rows (all loads in flight at once), 4 vectors
-// otherwise; the generic kernel for odd shapes and alignments.  FARN_VARIANT=bulk / stage / row / generic force
-// one of them; FARN_STAGE=0 leaves long inputs to the row kernel.
+// otherwise; the generic kernel for odd shapes and alignments.
+// FARN_VARIANT=bulk / stage / row / generic force one of them; FARN_STAGE=0
+// leaves long inputs to the row kernel.
 int make_moe_plan(const farn_ctx* ctx, int K, int64_t T, int64_t H, bool vec_ok, Plan* out) {
   Plan pl;
   pl.pb = 2; pl.cs = 1; pl.stages = 0; pl.stage_stride = 0; pl.smem = 0; pl.stage_r = 0;

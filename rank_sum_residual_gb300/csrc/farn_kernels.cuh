@@ -8,10 +8,14 @@
 // accumulation), fused into one pass over HBM.
 //
 // The page maps one token row to one CTA (Implementation section 2).  That
-// mapping is kept for long inputs (CS == 1).  For decode-sized T, where one
-// CTA per row would leave most of the 152 SMs idle, a thread-block cluster
-// of CS CTAs splits each row; the CTAs of a cluster exchange their partial
-// sums of squares through distributed shared memory (DSMEM).
+// mapping is kept for most calls (farn_vec_kernel with CS == 1).  For a
+// handful of rows, where one CTA per row would leave most of the 152 SMs
+// idle, a thread-block cluster of CS CTAs splits each row; the CTAs of a
+// cluster exchange their partial sums of squares through distributed
+// shared memory (DSMEM).  Long inputs of many partials, or with the
+// quantised outputs, take persistent kernels that stage the rows in shared
+// memory (farn_stage_kernel with cp.async, farn_bulk_kernel with TMA bulk
+// copies).
 //
 // Per element the arithmetic is fixed (f = exact bf16 -> fp32 widening,
 // bf16 = round to nearest even):
@@ -869,10 +873,12 @@ farn_combine_kernel(const __grid_constant__ Params p) {
 // nseg column segments of at most nct vectors (nct = the consumer threads).
 // A stage of the shared-memory ring holds one segment of every input of a
 // row: W+1 slots (x[0..W-1], then the residual) of p.stage_stride bytes.
-// Warp 0 is the producer: one thread streams the segments of this CTA's
-// rows, in order, into the ring -- per segment one expect_tx on the stage's
-// "full" mbarrier and W+1 cp.async.bulk copies (the TMA engine's bulk copy)
-// completing on it.  The other warps are the consumers: thread c owns
+// Warp 0 is the producer: it streams the segments of this CTA's rows, in
+// order, into the ring -- per segment lane 0 waits for the stage to be free
+// and posts one expect_tx on its "full" mbarrier, then lane r issues the
+// cp.async.bulk copy (the TMA engine's bulk copy) of input r, so the W+1
+// copies, completing on that barrier, go out side by side.  The other warps
+// are the consumers: thread c owns
 // vector c of every segment (vector k*nct + c of the row); per segment it
 // waits once for the stage, adds the W staged vectors in rank order, reads
 // the residual's, releases the stage (one arrival per warp on its "empty"
@@ -1513,7 +1519,9 @@ farn_stage_kernel(const __grid_constant__ Params p) {
 }
 
 // ------------------------------------ staged MoE combine (cp.async gather)
-// The MoE combine for long inputs, staged like farn_stage_kernel: each
+// The MoE combine for long inputs whose rows the TMA-staged kernel would
+// split into more than two segments of fewer than 256 consumers, staged
+// like farn_stage_kernel: each
 // persistent CTA walks its rows; the chunks of a row are its K gathered
 // expert rows (expert_out[index[t,k]]) and then its residual row; every
 // thread keeps R chunks of its own 16-byte vectors in flight with
