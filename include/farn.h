@@ -165,9 +165,9 @@ const char *farn_status_string(int status);
  * W < 8 with H <= 5120), 1 cluster (a cluster of CTAs splits each row; fewer than 16
  * rows), 2 generic (any H or alignment), 3 bulk (persistent CTAs whose
  * producer warp stages column segments of every input row in shared memory
- * with TMA bulk copies; rows of at most 16384 elements; long calls of
- * W >= 12 bf16 partials or of 8..11 with 5120 < H < 8192, or any call
- * when enabled), 4 stage (persistent CTAs whose threads stage their own
+ * with TMA bulk copies; rows of at most 16384 elements; calls of W >= 12
+ * bf16 partials from 256 rows, long calls of 8..11 with 5120 < H < 8192,
+ * or any call when enabled), 4 stage (persistent CTAs whose threads stage their own
  * vectors in shared memory with cp.async; the other long calls: 8..11
  * partials with H >= 8192, and the FP8 / NVFP4 outputs of W >= 3 partials
  * with H > 5120 or of W >= 8).

@@ -293,6 +293,7 @@ constexpr int64_t kClusterRowsMax = 16;
 // Long calls with at least this many bf16 inputs default to the TMA-staged
 // kernel (see make_plan).
 constexpr int kBulkDefaultMinW = 12;
+constexpr int64_t kBulkDefaultMinT = 256;
 // Long calls with fewer bf16 inputs and a bf16 norm_out take the row kernel
 // (see make_plan).
 constexpr int kStageMinW = 8;
@@ -416,8 +417,15 @@ int make_plan(const farn_ctx* ctx, int W, int64_t T, int64_t H, bool vec_ok, int
   const bool mid_w = W >= kStageMinW && W < kBulkDefaultMinW;
   const bool auto_long = want == kVariantAuto && ctx->force_cluster == 0 && ctx->stage &&
                          long_call(ctx, T, in_bytes);
+  // W >= 12 from 256 rows on, below the long-call threshold too (T = 256 /
+  // 512, W = 16, % of the copy bandwidth, TMA-staged against row: H = 4096,
+  // 61.7 / 77.3 against 51.2 / 77.3; H = 8192, 79.8 / 86.6 against 78.0 /
+  // 84.0).
+  const bool auto_mid = want == kVariantAuto && ctx->force_cluster == 0 && ctx->stage &&
+                        T >= kBulkDefaultMinT;
   const bool bulk_default =
-      auto_long && (W >= kBulkDefaultMinW || (mid_w && H > kRowMaxH && H < kStageMinH));
+      (auto_mid && W >= kBulkDefaultMinW) ||
+      (auto_long && mid_w && H > kRowMaxH && H < kStageMinH);
   const bool bulk_enabled = want == kVariantAuto && ctx->force_cluster == 0 && ctx->bulk && !small;
   if (vec_ok && pb == 2 && !quant &&
       (want == kVariantBulk || bulk_enabled || bulk_default) &&

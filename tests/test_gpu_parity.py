@@ -387,7 +387,9 @@ def test_plan_choices(dev):
         assert plan(8, 4096, 5120)[0] == "row"
         assert plan(10, 4096, 4096)[0] == "row"
         assert plan(8, 4096, 12288)[0] == "stage"
-        assert plan(16, 1000, 7168)[0] == "row"          # not a long call
+        assert plan(16, 1000, 7168)[0] == "bulk"         # W >= 12: from 256 rows on
+        assert plan(16, 255, 7168)[0] == "row"
+        assert plan(11, 1000, 7168)[0] == "row"          # 8..11: long calls only
         # half the row threshold when the call reads >= 128 MiB
         assert plan(8, 1024, 8192)[0] == "stage"        # 151 MB
         assert plan(8, 1023, 8192)[0] == "row"
